@@ -1,0 +1,156 @@
+/*
+ * gemma_attn.h -- C ABI of the mixed sliding/global attention step on a device-resident
+ * KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation: one attention step of a decoder whose layers interleave sliding-window
+ * and global attention ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", model family
+ * table and section 2.3), with grouped-query attention (same page, section 2.2: query
+ * head h reads KV head h / (n_q / n_kv)), cross-layer KV sharing (section 2.1: a shared
+ * layer attends against an earlier owner layer's cache and writes none), K used as V on
+ * layers with attention_k_eq_v ("Gemma-4 12B on AWS Inferentia2 - Tensor-Parallel (TP=2),
+ * device prefill", text config), and a one-token decode bucket plus a multi-token prefill
+ * bucket against a fixed-capacity cache that stays on the device and is updated in place
+ * (first page, section 5.1; "Gemma-4-E4B-it on AWS Inferentia2", "Decode neff").
+ *
+ * Definition computed (per sequence b, query token i, query head h):
+ *   len   = seq_lens[b]                      cache tokens after this step's append
+ *   p     = len - n_tok + i                  absolute position of the query
+ *   keys  = { j : j <= p, and p - j < window on a sliding layer }
+ *   out   = sum_j softmax_j(scale * q . K[j]) * V[j]   over those keys,
+ *   K, V  = the owner layer's cache, KV head h / (n_q / n_kv); V is K when k_eq_v.
+ *
+ * Conventions shared by every entry point
+ *  - The caller owns all memory. The library allocates nothing, never synchronises and
+ *    enqueues all work on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *    Every call can be captured in a CUDA graph.
+ *  - Pointers named "device" must be device-accessible (cudaMalloc'd) memory aligned to
+ *    16 bytes; arrays of pointers (k_cache, v_cache) and owner_map live in HOST memory.
+ *  - Cache layout, per owner layer: [batch][n_kv][kv_capacity][head_dim], row-major.
+ *    Query/output layout: [batch][n_tok][n_q][head_dim] (n_tok = 1 for decode).
+ *    New K/V rows: [batch][n_new][n_kv][head_dim]. Element type: `dtype` (bf16 or fp32;
+ *    fp32 is the debug build path); output has the same type.
+ *  - Argument errors are detected on the host before any launch and return a negative
+ *    gemma_status with nothing enqueued. A failed launch returns GEMMA_ERR_CUDA.
+ *  - Data-dependent errors (a seq_lens or write_pos entry out of range, only visible on
+ *    the device) never cause an out-of-bounds access: the affected sequence is skipped
+ *    (its output rows are written as zeros) and, when `device_error` is not NULL, a
+ *    GEMMA_DEVERR_* bit is OR-ed into that device word, which the caller reads after
+ *    synchronising. Internal waits are bounded and report GEMMA_DEVERR_TIMEOUT.
+ *  - Supported shapes: head_dim in {64, 128, 256, 512}; n_q / n_kv in {1, 2, 4, 8, 16};
+ *    window >= 1 on sliding layers. Others return GEMMA_ERR_UNSUPPORTED.
+ *  - batch == 0 or n_new == 0 is a valid empty call: GEMMA_OK, nothing enqueued.
+ */
+#ifndef GEMMA_ATTN_H
+#define GEMMA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMMA_SLIDING = 0, GEMMA_GLOBAL = 1 } gemma_layer_kind;
+typedef enum { GEMMA_BF16 = 0, GEMMA_FP32 = 1 } gemma_dtype;
+typedef enum {
+    GEMMA_OK = 0,
+    GEMMA_ERR_INVALID_ARG = -1,  /* NULL/misaligned pointer, bad owner map, inconsistent sizes */
+    GEMMA_ERR_UNSUPPORTED = -2,  /* head_dim or group size outside the supported set */
+    GEMMA_ERR_CAPACITY = -3,     /* max_seq_len / n_new beyond kv_capacity */
+    GEMMA_ERR_WORKSPACE = -4,    /* workspace NULL or smaller than gemma_attn_workspace_size */
+    GEMMA_ERR_CUDA = -5          /* a CUDA runtime call or launch failed */
+} gemma_status;
+
+/* Bits OR-ed into the optional device error word. */
+#define GEMMA_DEVERR_SEQ_LEN 1u    /* seq_lens[b] outside [n_tok, min(kv_capacity, max_seq_len)] */
+#define GEMMA_DEVERR_WRITE_POS 2u  /* write_pos[b] < 0 or write_pos[b] + n_new > kv_capacity */
+#define GEMMA_DEVERR_TIMEOUT 4u    /* an internal pipeline wait gave up */
+
+/*
+ * gemma_kv_append -- write this step's new K (and V) rows of an owner layer into its cache.
+ *   cache[b][h][write_pos[b] + t][:] = new[b][t][h][:]   for t < n_new, h < n_kv.
+ * Source: "Gemma-4-E4B-it on AWS Inferentia2" ("Decode neff": the KV buffers are updated in
+ * place each step) and the first page, section 2.1 (only owner layers hold a cache; shared
+ * layers never touch it). The pages' one-hot masked write is a tracing device of their
+ * compiler; here it is a direct scatter of whole rows.
+ *   k_cache, v_cache  HOST arrays [n_layers] of DEVICE cache pointers; entries of shared
+ *                     layers are never read. v_cache (and v_cache[layer]) may be NULL when
+ *                     k_eq_v, in which case v_new is ignored.
+ *   owner_map         HOST int32[n_layers]; if owner_map[layer] != layer the layer is
+ *                     shared and the call is a no-op returning GEMMA_OK.
+ *   k_new, v_new      DEVICE [batch][n_new][n_kv][head_dim].
+ *   write_pos         DEVICE int32[batch]: cache slot of the first new token of sequence b.
+ *   device_error      optional DEVICE uint32 (may be NULL).
+ */
+int gemma_kv_append(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
+                    int n_layers, int layer, const void* k_new, const void* v_new,
+                    const int32_t* write_pos, int batch, int n_new, int n_kv, int head_dim,
+                    int kv_capacity, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
+                    void* stream);
+
+/*
+ * gemma_attn_decode -- the decode bucket: one query token per sequence (n_tok = 1), whose
+ * K/V were appended first, so seq_lens[b] counts it. Source: first page, section 5.1
+ * ("decode: single-token forward against a fixed KV_MAX buffer").
+ *   out               DEVICE [batch][1][n_q][head_dim]   (written)
+ *   q                 DEVICE [batch][1][n_q][head_dim]
+ *   k_cache, v_cache  HOST arrays [n_layers] of DEVICE cache pointers; the layer reads
+ *                     k_cache[owner_map[layer]] (and v_cache[...] unless k_eq_v).
+ *   owner_map         HOST int32[n_layers]: 0 <= owner_map[l] <= l and
+ *                     owner_map[owner_map[l]] == owner_map[l]. The owner must have this
+ *                     layer's kind, n_kv, head_dim and k_eq_v (the caller's contract).
+ *   seq_lens          DEVICE int32[batch], 1 <= seq_lens[b] <= max_seq_len.
+ *   max_seq_len       HOST bound on seq_lens, used to plan the split over keys.
+ *   scale             softmax scale applied to q . k (1/sqrt(head_dim) in the workloads).
+ *   workspace         DEVICE scratch of at least
+ *                     gemma_attn_workspace_size(batch, kind, window, n_q, n_kv, head_dim,
+ *                     max_seq_len, 1) bytes (may be NULL when that size is 0). Contents on
+ *                     entry are ignored; concurrent calls must not share it.
+ */
+int gemma_attn_decode(void* out, const void* q, const void* const* k_cache,
+                      const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                      int layer, const int32_t* seq_lens, int max_seq_len, int batch,
+                      gemma_layer_kind kind, int window, int n_q, int n_kv, int head_dim,
+                      int k_eq_v, int kv_capacity, float scale, gemma_dtype dtype,
+                      void* workspace, size_t workspace_bytes, uint32_t* device_error,
+                      void* stream);
+
+/*
+ * gemma_attn_prefill -- the prefill bucket: n_new query tokens per sequence, written to the
+ * cache first (gemma_kv_append), at positions seq_lens[b] - n_new + i, attending causally
+ * (and within the window on sliding layers) over the cached prefix and the new tokens.
+ * Source: first page, section 5.1 ("prefill (padded prompt <= KV_BUCKET ...)") and the 12B
+ * model card ("a prefill bucket (seq = 64) and a decode bucket (seq = 1)"); here the bucket
+ * is exact (no pad rows) and may extend a cached prefix.
+ *   out, q            DEVICE [batch][n_new][n_q][head_dim]
+ *   seq_lens          DEVICE int32[batch], n_new <= seq_lens[b] <= max_seq_len.
+ *   Other arguments as for gemma_attn_decode (workspace sized with n_new).
+ */
+int gemma_attn_prefill(void* out, const void* q, const void* const* k_cache,
+                       const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                       int layer, const int32_t* seq_lens, int max_seq_len, int n_new,
+                       int batch, gemma_layer_kind kind, int window, int n_q, int n_kv,
+                       int head_dim, int k_eq_v, int kv_capacity, float scale,
+                       gemma_dtype dtype, void* workspace, size_t workspace_bytes,
+                       uint32_t* device_error, void* stream);
+
+/*
+ * gemma_attn_workspace_size -- bytes of scratch that gemma_attn_decode (n_new == 1) or
+ * gemma_attn_prefill (n_new > 1) needs for these arguments on the current device (the split
+ * plan depends on its SM count). Returns 0 when no scratch is needed and (size_t)-1 when the
+ * arguments are invalid.
+ */
+size_t gemma_attn_workspace_size(int batch, gemma_layer_kind kind, int window, int n_q,
+                                 int n_kv, int head_dim, int max_seq_len, int n_new);
+
+/* A static, human-readable name of a gemma_status value. */
+const char* gemma_status_string(int status);
+
+/* Version of this ABI (bumped on any signature change). */
+int gemma_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMMA_ATTN_H */

@@ -1,0 +1,248 @@
+// api.cu -- the C ABI declared in include/gemma_attn.h: host-side validation, owner-layer
+// resolution, the split plan of the decode bucket, and kernel launches. Nothing here
+// allocates memory or synchronises; every launch goes to the caller's stream.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/gemma_attn.h"
+#include "attn_internal.h"
+
+using gemma::RowsParams;
+
+namespace {
+
+constexpr int kMaxSplit = 128;
+constexpr int kMinChunkKeys = 256;  // keys per split chunk when work is plentiful
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return -1;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+bool group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+int check_shape(int kind, int window, int n_q, int n_kv, int head_dim, int dtype) {
+    if (kind != GEMMA_SLIDING && kind != GEMMA_GLOBAL) return GEMMA_ERR_INVALID_ARG;
+    if (kind == GEMMA_SLIDING && window < 1) return GEMMA_ERR_INVALID_ARG;
+    if (n_q < 1 || n_kv < 1 || n_q % n_kv != 0) return GEMMA_ERR_INVALID_ARG;
+    if (dtype != GEMMA_BF16 && dtype != GEMMA_FP32) return GEMMA_ERR_INVALID_ARG;
+    if (!head_dim_ok(head_dim) || !group_ok(n_q / n_kv)) return GEMMA_ERR_UNSUPPORTED;
+    return GEMMA_OK;
+}
+
+// Owner resolution ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", section 2.1): a
+// layer reads the cache of owner_map[layer], an earlier layer that owns its cache.
+int resolve_owner(const int32_t* owner_map, int n_layers, int layer, int* owner) {
+    if (!owner_map || n_layers < 1 || layer < 0 || layer >= n_layers) return GEMMA_ERR_INVALID_ARG;
+    const int o = owner_map[layer];
+    if (o < 0 || o > layer || owner_map[o] != o) return GEMMA_ERR_INVALID_ARG;
+    *owner = o;
+    return GEMMA_OK;
+}
+
+struct Plan {
+    int n_split;
+    int chunk;
+    size_t o_bytes;   // partial outputs
+    size_t ws_bytes;  // total scratch
+};
+
+// Decode splits each (sequence, KV head) key range into chunks so that enough CTAs stream
+// the cache at once: about one chunk per SM for small problems, about eight per SM (and at
+// least kMinChunkKeys keys each) for large ones. Prefill has one row tile per 16 rows and no
+// split. Depends only on the arguments and the SM count.
+Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim, int max_seq_len,
+               int n_tok, int n_sm) {
+    Plan pl{1, 1 << 30, 0, 0};
+    if (n_tok != 1) return pl;
+    const long long T = gemma::kKeyTile;
+    const long long n_read = kind == GEMMA_SLIDING && window < max_seq_len ? window : max_seq_len;
+    const long long total = (long long)batch * n_kv * n_read;
+    const long long one_per_sm = round_up((total + n_sm - 1) / n_sm, T);
+    const long long eight_per_sm = round_up((total + 8LL * n_sm - 1) / (8LL * n_sm), T);
+    long long chunk = one_per_sm < kMinChunkKeys ? one_per_sm : kMinChunkKeys;
+    if (eight_per_sm > chunk) chunk = eight_per_sm;
+    if (chunk < T) chunk = T;
+    long long n_split = (n_read + chunk - 1) / chunk;
+    if (n_split > kMaxSplit) {
+        chunk = round_up((n_read + kMaxSplit - 1) / kMaxSplit, T);
+        n_split = (n_read + chunk - 1) / chunk;
+    }
+    if (n_split <= 1) return pl;
+    pl.n_split = (int)n_split;
+    pl.chunk = (int)chunk;
+    const size_t rows = (size_t)batch * n_q * n_split;
+    pl.o_bytes = (size_t)round_up((long long)(rows * head_dim * sizeof(float)), 256);
+    pl.ws_bytes = pl.o_bytes + (size_t)round_up((long long)(rows * 2 * sizeof(float)), 256);
+    return pl;
+}
+
+int attention(void* out, const void* q, const void* const* k_cache, const void* const* v_cache,
+              const int32_t* owner_map, int n_layers, int layer, const int32_t* seq_lens,
+              int max_seq_len, int n_tok, int batch, int kind, int window, int n_q, int n_kv,
+              int head_dim, int k_eq_v, int kv_capacity, float scale, int dtype, void* workspace,
+              size_t workspace_bytes, uint32_t* device_error, void* stream) {
+    if (batch < 0 || n_tok < 1) return GEMMA_ERR_INVALID_ARG;
+    int st = check_shape(kind, window, n_q, n_kv, head_dim, dtype);
+    if (st != GEMMA_OK) return st;
+    int o = 0;
+    st = resolve_owner(owner_map, n_layers, layer, &o);
+    if (st != GEMMA_OK) return st;
+    if (kv_capacity < 1 || max_seq_len < n_tok || !std::isfinite(scale)) return GEMMA_ERR_INVALID_ARG;
+    if (max_seq_len > kv_capacity) return GEMMA_ERR_CAPACITY;
+    if (batch > 65535) return GEMMA_ERR_UNSUPPORTED;
+    if (batch == 0) return GEMMA_OK;
+    if (!out || !q || !seq_lens || !k_cache || !k_cache[o]) return GEMMA_ERR_INVALID_ARG;
+    const void* kc = k_cache[o];
+    const void* vc = kc;
+    if (!k_eq_v) {
+        if (!v_cache || !v_cache[o]) return GEMMA_ERR_INVALID_ARG;
+        vc = v_cache[o];
+    }
+    if (!aligned16(out) || !aligned16(q) || !aligned16(kc) || !aligned16(vc))
+        return GEMMA_ERR_INVALID_ARG;
+    const int n_sm = sm_count();
+    if (n_sm < 0) return GEMMA_ERR_CUDA;
+    const Plan pl = make_plan(batch, kind, window, n_q, n_kv, head_dim, max_seq_len, n_tok, n_sm);
+    if (pl.ws_bytes > 0 &&
+        (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace)))
+        return GEMMA_ERR_WORKSPACE;
+
+    RowsParams p{};
+    p.q = q;
+    p.k = kc;
+    p.v = vc;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.o_part = pl.ws_bytes ? static_cast<float*>(workspace) : nullptr;
+    p.ml_part = pl.ws_bytes
+                    ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.o_bytes)
+                    : nullptr;
+    p.err = device_error;
+    p.n_tok = n_tok;
+    p.n_q = n_q;
+    p.n_kv = n_kv;
+    p.G = n_q / n_kv;
+    p.cap = kv_capacity;
+    p.window = window;
+    p.is_sliding = kind == GEMMA_SLIDING;
+    p.k_eq_v = k_eq_v ? 1 : 0;
+    p.max_seq_len = max_seq_len;
+    p.n_split = pl.n_split;
+    p.chunk = pl.chunk;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long rows = (long long)n_tok * p.G;
+    cudaError_t e;
+    if (dtype == GEMMA_BF16) {
+        const size_t smem = gemma::rows_bf16_smem_bytes(head_dim, p.k_eq_v, &p.n_stages);
+        const long long tiles = (rows + gemma::kRowTile - 1) / gemma::kRowTile;
+        e = gemma::launch_rows_bf16(p, head_dim, dim3((unsigned)(tiles * pl.n_split), n_kv, batch),
+                                    smem, s);
+    } else {
+        const long long tiles = (rows + gemma::kF32RowsPerCta - 1) / gemma::kF32RowsPerCta;
+        e = gemma::launch_rows_f32(p, head_dim, dim3((unsigned)(tiles * pl.n_split), n_kv, batch),
+                                   s);
+    }
+    if (e == cudaSuccess && pl.n_split > 1)
+        e = gemma::launch_combine(p, head_dim, batch, dtype == GEMMA_FP32, s);
+    return e == cudaSuccess ? GEMMA_OK : GEMMA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemma_abi_version(void) { return 1; }
+
+const char* gemma_status_string(int status) {
+    switch (status) {
+        case GEMMA_OK: return "GEMMA_OK";
+        case GEMMA_ERR_INVALID_ARG: return "GEMMA_ERR_INVALID_ARG";
+        case GEMMA_ERR_UNSUPPORTED: return "GEMMA_ERR_UNSUPPORTED";
+        case GEMMA_ERR_CAPACITY: return "GEMMA_ERR_CAPACITY";
+        case GEMMA_ERR_WORKSPACE: return "GEMMA_ERR_WORKSPACE";
+        case GEMMA_ERR_CUDA: return "GEMMA_ERR_CUDA";
+    }
+    return "GEMMA_UNKNOWN_STATUS";
+}
+
+int gemma_kv_append(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
+                    int n_layers, int layer, const void* k_new, const void* v_new,
+                    const int32_t* write_pos, int batch, int n_new, int n_kv, int head_dim,
+                    int kv_capacity, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
+                    void* stream) {
+    if (batch < 0 || n_new < 0 || n_kv < 1 || kv_capacity < 1) return GEMMA_ERR_INVALID_ARG;
+    if (dtype != GEMMA_BF16 && dtype != GEMMA_FP32) return GEMMA_ERR_INVALID_ARG;
+    if (!head_dim_ok(head_dim)) return GEMMA_ERR_UNSUPPORTED;
+    int o = 0;
+    int st = resolve_owner(owner_map, n_layers, layer, &o);
+    if (st != GEMMA_OK) return st;
+    if (o != layer) return GEMMA_OK;  // a shared layer writes no cache
+    if (n_new > kv_capacity) return GEMMA_ERR_CAPACITY;
+    if (batch == 0 || n_new == 0) return GEMMA_OK;
+    if (!k_cache || !k_cache[layer] || !k_new || !write_pos) return GEMMA_ERR_INVALID_ARG;
+    void* vc = nullptr;
+    if (!k_eq_v) {
+        if (!v_cache || !v_cache[layer] || !v_new) return GEMMA_ERR_INVALID_ARG;
+        vc = v_cache[layer];
+    }
+    if (!aligned16(k_cache[layer]) || !aligned16(k_new) ||
+        (vc && (!aligned16(vc) || !aligned16(v_new))))
+        return GEMMA_ERR_INVALID_ARG;
+    const int n_sm = sm_count();
+    if (n_sm < 0) return GEMMA_ERR_CUDA;
+    const int row_bytes = head_dim * (dtype == GEMMA_BF16 ? 2 : 4);
+    cudaError_t e = gemma::launch_kv_append(k_cache[layer], vc, k_new, vc ? v_new : nullptr,
+                                            write_pos, batch, n_new, n_kv, kv_capacity, row_bytes,
+                                            device_error, n_sm, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GEMMA_OK : GEMMA_ERR_CUDA;
+}
+
+int gemma_attn_decode(void* out, const void* q, const void* const* k_cache,
+                      const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                      int layer, const int32_t* seq_lens, int max_seq_len, int batch,
+                      gemma_layer_kind kind, int window, int n_q, int n_kv, int head_dim,
+                      int k_eq_v, int kv_capacity, float scale, gemma_dtype dtype,
+                      void* workspace, size_t workspace_bytes, uint32_t* device_error,
+                      void* stream) {
+    return attention(out, q, k_cache, v_cache, owner_map, n_layers, layer, seq_lens, max_seq_len,
+                     1, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
+                     dtype, workspace, workspace_bytes, device_error, stream);
+}
+
+int gemma_attn_prefill(void* out, const void* q, const void* const* k_cache,
+                       const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                       int layer, const int32_t* seq_lens, int max_seq_len, int n_new,
+                       int batch, gemma_layer_kind kind, int window, int n_q, int n_kv,
+                       int head_dim, int k_eq_v, int kv_capacity, float scale,
+                       gemma_dtype dtype, void* workspace, size_t workspace_bytes,
+                       uint32_t* device_error, void* stream) {
+    if (n_new == 0 && batch >= 0) return GEMMA_OK;
+    return attention(out, q, k_cache, v_cache, owner_map, n_layers, layer, seq_lens, max_seq_len,
+                     n_new, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
+                     dtype, workspace, workspace_bytes, device_error, stream);
+}
+
+size_t gemma_attn_workspace_size(int batch, gemma_layer_kind kind, int window, int n_q,
+                                 int n_kv, int head_dim, int max_seq_len, int n_new) {
+    if (batch < 0 || n_new < 1 || max_seq_len < n_new) return (size_t)-1;
+    if (check_shape(kind, window, n_q, n_kv, head_dim, GEMMA_BF16) != GEMMA_OK) return (size_t)-1;
+    if (batch == 0) return 0;
+    const int n_sm = sm_count();
+    if (n_sm < 0) return (size_t)-1;
+    return make_plan(batch, kind, window, n_q, n_kv, head_dim, max_seq_len, n_new, n_sm).ws_bytes;
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// attn_internal.h -- launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gemma {
+
+// One attention launch over "rows": a row is one (query token, query head) pair. Rows are
+// ordered token-major, then by the head's index inside its GQA group, so a tile of rows
+// shares one KV head. Decode has one token (rows = the G heads of a group); prefill has n_tok
+// tokens per sequence.
+struct RowsParams {
+    const void* q;            // [B][n_tok][n_q][D]
+    const void* k;            // owner layer's K cache [B][n_kv][cap][D]
+    const void* v;            // owner layer's V cache (== k when k_eq_v)
+    const int32_t* seq_lens;  // [B], tokens in the cache after this step's append
+    void* out;                // [B][n_tok][n_q][D], written when n_split == 1
+    float* o_part;            // [B][n_q][n_split][D]  unnormalised partial outputs
+    float* ml_part;           // [B][n_q][n_split][2]  (running max in log2 units, sum)
+    uint32_t* err;            // optional device error word
+    int n_tok, n_q, n_kv, G, cap, window, is_sliding, k_eq_v;
+    int max_seq_len;
+    int n_split;              // key chunks per row tile (1: write `out` directly)
+    int chunk;                // keys per chunk (multiple of the key tile)
+    int n_stages;             // smem pipeline depth (bf16 kernel)
+    float scale_log2;         // softmax scale * log2(e)
+    float scale;              // softmax scale
+};
+
+// Keys per shared-memory tile of the bf16 kernel; chunks are multiples of it.
+constexpr int kKeyTile = 32;
+constexpr int kRowTile = 16;     // rows per CTA in the bf16 kernel (one m16 MMA tile)
+constexpr int kF32RowsPerCta = 4;
+
+size_t rows_bf16_smem_bytes(int head_dim, int k_eq_v, int* n_stages);
+cudaError_t launch_rows_bf16(const RowsParams& p, int head_dim, dim3 grid, size_t smem,
+                             cudaStream_t st);
+cudaError_t launch_rows_f32(const RowsParams& p, int head_dim, dim3 grid, cudaStream_t st);
+cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out_fp32,
+                           cudaStream_t st);
+cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                             const int32_t* write_pos, int batch, int n_new, int n_kv,
+                             int capacity, int row_bytes, uint32_t* err, int n_sm,
+                             cudaStream_t st);
+
+}  // namespace gemma

@@ -1,0 +1,547 @@
+// rows_attn.cu -- attention over a device-resident KV cache for tiles of query rows.
+//
+// Serves the decode bucket (one token per sequence, split over key chunks, partials merged
+// by combine_kernel) and the prefill bucket (many tokens per sequence, one pass per row
+// tile). Definition ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", sections 2.1-2.3
+// and 4.3): query head h of a layer reads KV head h / G of the owner layer's cache; the query
+// at absolute position p attends keys j <= p, and on a sliding layer only p - j < window; the
+// output is softmax(scale * q k^T) v over those keys, with V = K on k_eq_v layers.
+//
+// bf16 kernel design (per CTA: one KV head of one sequence, 16 query rows, one key chunk):
+//  - the key range is clamped to the window / causal limit before any load (no predicated
+//    loads of keys the tile cannot attend);
+//  - a producer warp streams 32-key K/V tiles with TMA bulk copies (one per cache row, so
+//    only the rows in range are read) into a shared-memory ring with padded rows, so the
+//    ldmatrix reads below are bank-conflict free; every K/V tile is read from HBM once and
+//    reused by all rows (all query heads of the GQA group, and all tokens of the tile);
+//  - eight consumer warps: (1) S = Q K^T with mma.sync m16n8k16 (warps split keys x head_dim),
+//    (2) per-row online softmax in exp2 form with warp shuffles, P rounded to bf16,
+//    (3) O = diag(alpha) O + P V (warps split head_dim);
+//  - fp32 accumulation throughout; partial (m, l, O) per chunk when the keys are split.
+#include "attn_internal.h"
+#include "common.cuh"
+
+namespace gemma {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kRowsThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 113 * 1024;  // two CTAs per SM
+
+template <int D>
+struct RowsLayout {
+    static constexpr int ROW = 2 * D + 16;  // padded bytes per cache row in shared memory
+    static constexpr int TILE = kKeyTile * ROW;
+    static constexpr int KSPLIT = D >= 512 ? 4 : 2;  // warps sharing one n-tile in S = QK^T
+    static constexpr int S_STRIDE = kKeyTile + 8;    // fp32 words per S row
+    static constexpr int P_STRIDE = kKeyTile + 8;    // bf16 elements per P row
+    static constexpr int Q_OFF = 0;
+    static constexpr int S_OFF = Q_OFF + kRowTile * ROW;
+    static constexpr int P_OFF = S_OFF + KSPLIT * kRowTile * S_STRIDE * 4;
+    static constexpr int STAT_OFF = P_OFF + kRowTile * P_STRIDE * 2;  // alpha, m, l [16] each
+    static constexpr int BAR_OFF = (STAT_OFF + 3 * kRowTile * 4 + 15) / 16 * 16;
+    static constexpr int RING_OFF = (BAR_OFF + 2 * kMaxStages * 8 + 127) / 128 * 128;
+};
+
+// Row geometry: local row r of tile rt is global row R = rt*16 + r, token R / G, member R % G.
+struct RowInfo {
+    int token, head, pos, lo;
+};
+
+GEMMA_DEVINL RowInfo row_info(const RowsParams& p, int len, int kvh, int R) {
+    RowInfo ri;
+    ri.token = R / p.G;
+    ri.head = kvh * p.G + (R - ri.token * p.G);
+    ri.pos = len - p.n_tok + ri.token;
+    ri.lo = p.is_sliding ? max(0, ri.pos - p.window + 1) : 0;
+    return ri;
+}
+
+template <typename OutT>
+GEMMA_DEVINL void zero_rows(const RowsParams& p, int b, int kvh, int row0, int n_rows, int D) {
+    const int vec = 16 / (int)sizeof(OutT);
+    const int per_row = D / vec;
+    for (int idx = threadIdx.x; idx < n_rows * per_row; idx += blockDim.x) {
+        const int r = idx / per_row, ch = idx - r * per_row;
+        const int R = row0 + r;
+        const int token = R / p.G, head = kvh * p.G + (R - token * p.G);
+        OutT* dst = reinterpret_cast<OutT*>(p.out) +
+                    (((size_t)b * p.n_tok + token) * p.n_q + head) * (size_t)D + (size_t)ch * vec;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kRowsThreads, 2) rows_attn_bf16_kernel(const RowsParams p) {
+    using Lay = RowsLayout<D>;
+    constexpr int T = kKeyTile;
+    constexpr int KSPLIT = Lay::KSPLIT;
+    constexpr int NGROUPS = kConsumerWarps / KSPLIT;  // n-groups of S columns
+    constexpr int NTW = (T / 8) / NGROUPS;            // 8-key n-tiles per warp in S
+    constexpr int KS = D / KSPLIT / 16;               // 16-wide k-steps per warp in S
+    constexpr int NB = D / 8 / 8;                     // 8-column n-tiles per warp in O
+    static_assert(KS % 2 == 0 && NTW >= 1, "tile shape");
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x % p.n_split;
+    const int rt = blockIdx.x / p.n_split;
+    const int kvh = blockIdx.y, b = blockIdx.z;
+    const int rows_total = p.n_tok * p.G;
+    const int row0 = rt * kRowTile;
+    const int n_rows = min(kRowTile, rows_total - row0);
+    const bool direct = p.n_split == 1;
+    const int len = __ldg(p.seq_lens + b);
+
+    if (len < p.n_tok || len > p.cap || len > p.max_seq_len) {
+        if (split == 0) {
+            if (threadIdx.x == 0) report(p.err, GEMMA_DEVERR_SEQ_LEN);
+            if (direct) zero_rows<__nv_bfloat16>(p, b, kvh, row0, n_rows, D);
+        }
+        return;
+    }
+    // keys any row of this tile may attend, then this CTA's chunk of them
+    const RowInfo first = row_info(p, len, kvh, row0);
+    const RowInfo last = row_info(p, len, kvh, row0 + n_rows - 1);
+    const int kb = first.lo + split * p.chunk;
+    const int ke = min(last.pos + 1, kb + p.chunk);
+    if (kb >= ke) return;  // empty chunk: the combine pass skips it
+    const int n_keys = ke - kb;
+    const int n_tiles = (n_keys + T - 1) / T;
+    const int nops = p.k_eq_v ? 1 : 2;
+    const int stage_bytes = nops * Lay::TILE;
+    const int S = p.n_stages;
+
+    uint8_t* sQ = smem + Lay::Q_OFF;
+    float* sS = reinterpret_cast<float*>(smem + Lay::S_OFF);
+    __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(smem + Lay::P_OFF);
+    float* sAlpha = reinterpret_cast<float*>(smem + Lay::STAT_OFF);
+    float* sM = sAlpha + kRowTile;
+    float* sL = sM + kRowTile;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFF);
+    uint64_t* empty = full + kMaxStages;
+    uint8_t* ring = smem + Lay::RING_OFF;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    // Q rows of the tile (zero beyond n_rows), P = 0, row statistics
+    {
+        const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q);
+        constexpr int CH = D / 8;
+        for (int idx = threadIdx.x; idx < kRowTile * CH; idx += blockDim.x) {
+            const int r = idx / CH, ch = idx - r * CH;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < n_rows) {
+                const RowInfo ri = row_info(p, len, kvh, row0 + r);
+                v = __ldg(reinterpret_cast<const uint4*>(
+                    q + (((size_t)b * p.n_tok + ri.token) * p.n_q + ri.head) * (size_t)D + ch * 8));
+            }
+            *reinterpret_cast<uint4*>(sQ + r * Lay::ROW + ch * 16) = v;
+        }
+        uint32_t* p32 = reinterpret_cast<uint32_t*>(sP);
+        for (int idx = threadIdx.x; idx < kRowTile * Lay::P_STRIDE / 2; idx += blockDim.x)
+            p32[idx] = 0u;
+        if (threadIdx.x < 3 * kRowTile) sAlpha[threadIdx.x] = 0.f;
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer warp: TMA bulk copies of the K/V rows in range ----------------
+        const size_t head_base = ((size_t)b * p.n_kv + kvh) * (size_t)p.cap + (size_t)kb;
+        const uint8_t* kg = reinterpret_cast<const uint8_t*>(p.k) + head_base * (2 * D);
+        const uint8_t* vg = reinterpret_cast<const uint8_t*>(p.v) + head_base * (2 * D);
+        for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % S;
+            if (t >= S && !mbar_wait(&empty[s], ((t / S) - 1) & 1, p.err)) break;
+            const int rows = min(T, n_keys - t * T);
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(rows * 2 * D * nops));
+            __syncwarp();
+            uint8_t* dk = ring + s * stage_bytes;
+            for (int r = lane; r < rows; r += 32) {
+                const size_t off = (size_t)(t * T + r) * (2 * D);
+                bulk_g2s(dk + r * Lay::ROW, kg + off, 2 * D, &full[s]);
+                if (nops == 2) bulk_g2s(dk + Lay::TILE + r * Lay::ROW, vg + off, 2 * D, &full[s]);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------- consumer warps ----------------------------------------
+    const int ng = warp % NGROUPS;  // S columns [ng*NTW*8, +NTW*8)
+    const int kp = warp / NGROUPS;  // head_dim part [kp*D/KSPLIT, +D/KSPLIT)
+    const int g = lane >> 2, tq = lane & 3;
+
+    uint32_t qa[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const int d0 = kp * (D / KSPLIT) + ks * 16;
+        const uint32_t addr = smem_u32(sQ + (lane & 15) * Lay::ROW + (d0 + (lane >> 4) * 8) * 2);
+        ldsm_x4(addr, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+    }
+
+    // rows owned by this warp in the softmax step: warp and warp + 8
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    int r_lo[2], r_hi[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int r = warp + 8 * rr;
+        if (r < n_rows) {
+            const RowInfo ri = row_info(p, len, kvh, row0 + r);
+            r_lo[rr] = ri.lo;
+            r_hi[rr] = ri.pos + 1;
+        } else {
+            r_lo[rr] = 1;
+            r_hi[rr] = 0;
+        }
+    }
+
+    float o[NB][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+    // A wait that gives up (recorded in the error word) makes this warp stop waiting but keep
+    // walking the tile loop, so every consumer warp still reaches every named barrier.
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % S;
+        if (ok) ok = mbar_wait(&full[s], (t / S) & 1, p.err);
+        const uint8_t* tK = ring + s * stage_bytes;
+        const uint8_t* tV = nops == 2 ? tK + Lay::TILE : tK;
+        const int rows_valid = min(T, n_keys - t * T);
+
+        // (1) partial S over this warp's head_dim part
+        {
+            float sacc[NTW][4];
+#pragma unroll
+            for (int j = 0; j < NTW; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+#pragma unroll
+            for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
+                const int d0 = kp * (D / KSPLIT) + ks2 * 32;
+#pragma unroll
+                for (int j = 0; j < NTW; ++j) {
+                    const int key = (ng * NTW + j) * 8 + (lane & 7);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(smem_u32(tK + key * Lay::ROW + (d0 + (lane >> 3) * 8) * 2), b0, b1, b2,
+                            b3);
+                    mma_bf16(sacc[j], qa[2 * ks2][0], qa[2 * ks2][1], qa[2 * ks2][2],
+                             qa[2 * ks2][3], b0, b1);
+                    mma_bf16(sacc[j], qa[2 * ks2 + 1][0], qa[2 * ks2 + 1][1], qa[2 * ks2 + 1][2],
+                             qa[2 * ks2 + 1][3], b2, b3);
+                }
+            }
+            float* Sk = sS + kp * kRowTile * Lay::S_STRIDE;
+#pragma unroll
+            for (int j = 0; j < NTW; ++j) {
+                const int col = (ng * NTW + j) * 8 + 2 * tq;
+                *reinterpret_cast<float2*>(Sk + g * Lay::S_STRIDE + col) =
+                    make_float2(sacc[j][0], sacc[j][1]);
+                *reinterpret_cast<float2*>(Sk + (g + 8) * Lay::S_STRIDE + col) =
+                    make_float2(sacc[j][2], sacc[j][3]);
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+
+        // (2) online softmax of rows warp and warp + 8: lane = key of the tile
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int r = warp + 8 * rr;
+            if (r < n_rows) {
+                const int key = kb + t * T + lane;
+                const bool valid = lane < rows_valid && key >= r_lo[rr] && key < r_hi[rr];
+                float sv = 0.f;
+#pragma unroll
+                for (int kq = 0; kq < KSPLIT; ++kq)
+                    sv += sS[(kq * kRowTile + r) * Lay::S_STRIDE + lane];
+                sv = valid ? sv * p.scale_log2 : -INFINITY;
+                const float m_new = fmaxf(m_run[rr], warp_max(sv));
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = exp2f(m_run[rr] - m_use);
+                const __nv_bfloat16 pb = __float2bfloat16_rn(exp2f(sv - m_use));
+                sP[r * Lay::P_STRIDE + lane] = pb;
+                l_run[rr] = l_run[rr] * alpha + warp_sum(__bfloat162float(pb));
+                m_run[rr] = m_new;
+                if (lane == 0) sAlpha[r] = alpha;
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+
+        // (3) O = diag(alpha) O + P V over this warp's columns [warp*D/8, +D/8)
+        {
+            const float a_lo = sAlpha[g], a_hi = sAlpha[g + 8];
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                o[j][0] *= a_lo;
+                o[j][1] *= a_lo;
+                o[j][2] *= a_hi;
+                o[j][3] *= a_hi;
+            }
+#pragma unroll
+            for (int kk = 0; kk < T / 16; ++kk) {
+                uint32_t pa0, pa1, pa2, pa3;
+                ldsm_x4(smem_u32(sP + (lane & 15) * Lay::P_STRIDE + kk * 16 + (lane >> 4) * 8), pa0,
+                        pa1, pa2, pa3);
+                // keys of this thread's B fragment halves: k0, k0+1 (low) and k0+8, k0+9 (high)
+                const int k0 = kk * 16 + 2 * tq;
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (rows_valid < T) {  // rows past the tile's end were not loaded: zero them
+                    mlo = (k0 < rows_valid ? 0x0000ffffu : 0u) | (k0 + 1 < rows_valid ? 0xffff0000u : 0u);
+                    mhi = (k0 + 8 < rows_valid ? 0x0000ffffu : 0u) |
+                          (k0 + 9 < rows_valid ? 0xffff0000u : 0u);
+                }
+                const int vkey = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int j = 0; j < NB; j += 2) {
+                    const int col = warp * (D / 8) + j * 8 + (lane >> 4) * 8;
+                    if (j + 1 < NB) {
+                        uint32_t v0, v1, v2, v3;
+                        ldsm_x4_t(smem_u32(tV + vkey * Lay::ROW + col * 2), v0, v1, v2, v3);
+                        mma_bf16(o[j], pa0, pa1, pa2, pa3, v0 & mlo, v1 & mhi);
+                        mma_bf16(o[j + 1], pa0, pa1, pa2, pa3, v2 & mlo, v3 & mhi);
+                    } else {
+                        uint32_t v0, v1;
+                        const int c1 = warp * (D / 8) + j * 8;
+                        asm volatile(
+                            "ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                            : "=r"(v0), "=r"(v1)
+                            : "r"(smem_u32(tV + vkey * Lay::ROW + c1 * 2)));
+                        mma_bf16(o[j], pa0, pa1, pa2, pa3, v0 & mlo, v1 & mhi);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ------------------------------------- epilogue -------------------------------------------
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int r = warp + 8 * rr;
+        if (r < n_rows && lane == 0) {
+            sM[r] = m_run[rr];
+            sL[r] = l_run[rr];
+        }
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = g + 8 * half;
+        if (r >= n_rows) continue;
+        const RowInfo ri = row_info(p, len, kvh, row0 + r);
+        if (direct) {
+            const float inv = 1.f / sL[r];
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                 (((size_t)b * p.n_tok + ri.token) * p.n_q + ri.head) * (size_t)D;
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                const int col = warp * (D / 8) + j * 8 + 2 * tq;
+                *reinterpret_cast<uint32_t*>(dst + col) =
+                    pack_bf16(o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
+            }
+        } else {
+            const size_t pr = ((size_t)b * p.n_q + ri.head) * p.n_split + split;
+            float* dst = p.o_part + pr * D;
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                const int col = warp * (D / 8) + j * 8 + 2 * tq;
+                *reinterpret_cast<float2*>(dst + col) = make_float2(o[j][2 * half], o[j][2 * half + 1]);
+            }
+            if (warp == 0 && tq == 0) {
+                p.ml_part[pr * 2 + 0] = sM[r];
+                p.ml_part[pr * 2 + 1] = sL[r];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// fp32 debug path: one warp per row, lanes split head_dim, FFMA with expf (accuracy first).
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(const RowsParams p) {
+    constexpr int E = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x % p.n_split;
+    const int rt = blockIdx.x / p.n_split;
+    const int kvh = blockIdx.y, b = blockIdx.z;
+    const int R = rt * kF32RowsPerCta + warp;
+    if (R >= p.n_tok * p.G) return;
+    const int len = __ldg(p.seq_lens + b);
+    const bool direct = p.n_split == 1;
+    const int token = R / p.G, head = kvh * p.G + (R - token * p.G);
+    float* out_row = reinterpret_cast<float*>(p.out) +
+                     (((size_t)b * p.n_tok + token) * p.n_q + head) * (size_t)D;
+    if (len < p.n_tok || len > p.cap || len > p.max_seq_len) {
+        if (split == 0) {
+            if (lane == 0) report(p.err, GEMMA_DEVERR_SEQ_LEN);
+            if (direct)
+                for (int e = 0; e < E; ++e) out_row[lane + 32 * e] = 0.f;
+        }
+        return;
+    }
+    const int pos = len - p.n_tok + token;
+    const int lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
+    const int kb = lo + split * p.chunk;
+    const int ke = min(pos + 1, kb + p.chunk);
+    if (kb >= ke) return;
+
+    const float* q = reinterpret_cast<const float*>(p.q) +
+                     (((size_t)b * p.n_tok + token) * p.n_q + head) * (size_t)D;
+    const size_t hb = ((size_t)b * p.n_kv + kvh) * (size_t)p.cap;
+    const float* K = reinterpret_cast<const float*>(p.k) + hb * D;
+    const float* V = reinterpret_cast<const float*>(p.v) + hb * D;
+    float qr[E], acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        qr[e] = q[lane + 32 * e];
+        acc[e] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    for (int j = kb; j < ke; ++j) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot = fmaf(qr[e], K[(size_t)j * D + lane + 32 * e], dot);
+        const float s = warp_sum(dot) * p.scale;
+        const float m_new = fmaxf(m, s);
+        const float alpha = expf(m - m_new);
+        const float w = expf(s - m_new);
+        l = l * alpha + w;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, V[(size_t)j * D + lane + 32 * e], acc[e] * alpha);
+        m = m_new;
+    }
+    if (direct) {
+        const float inv = 1.f / l;
+#pragma unroll
+        for (int e = 0; e < E; ++e) out_row[lane + 32 * e] = acc[e] * inv;
+    } else {
+        const size_t pr = ((size_t)b * p.n_q + head) * p.n_split + split;
+#pragma unroll
+        for (int e = 0; e < E; ++e) p.o_part[pr * D + lane + 32 * e] = acc[e];
+        if (lane == 0) {
+            p.ml_part[pr * 2 + 0] = m * 1.4426950408889634f;  // natural -> log2 units
+            p.ml_part[pr * 2 + 1] = l;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// split-K combine (decode): merge the per-chunk (m, l, O) of each (sequence, query head)
+//   M = max_c m_c,  w_c = 2^(m_c - M),  out = sum_c w_c O_c / sum_c w_c l_c
+// ---------------------------------------------------------------------------------------------
+template <typename OutT>
+__global__ void combine_kernel(const RowsParams p, int D) {
+    const int head = blockIdx.x, b = blockIdx.y;
+    const int len = __ldg(p.seq_lens + b);
+    OutT* dst = reinterpret_cast<OutT*>(p.out) + ((size_t)b * p.n_q + head) * (size_t)D;
+    const int col = threadIdx.x * 4;
+    if (len < 1 || len > p.cap || len > p.max_seq_len) {
+        if (col < D)
+            for (int e = 0; e < 4; ++e) dst[col + e] = OutT(0.f);
+        return;
+    }
+    const int lo = p.is_sliding ? max(0, len - p.window) : 0;
+    const int nc = min(p.n_split, (len - lo + p.chunk - 1) / p.chunk);
+    const size_t base = ((size_t)b * p.n_q + head) * p.n_split;
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, p.ml_part[(base + c) * 2]);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < nc; ++c) {
+        const float w = exp2f(p.ml_part[(base + c) * 2] - M);
+        L = fmaf(w, p.ml_part[(base + c) * 2 + 1], L);
+        if (col < D) {
+            const float4 v = *reinterpret_cast<const float4*>(p.o_part + (base + c) * D + col);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+    }
+    if (col < D) {
+        const float inv = 1.f / L;
+        dst[col + 0] = OutT(acc.x * inv);
+        dst[col + 1] = OutT(acc.y * inv);
+        dst[col + 2] = OutT(acc.z * inv);
+        dst[col + 3] = OutT(acc.w * inv);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------------------------
+template <int D>
+static size_t smem_for(int k_eq_v, int* n_stages) {
+    using Lay = RowsLayout<D>;
+    const int stage = (k_eq_v ? 1 : 2) * Lay::TILE;
+    int s = (kSmemBudget - Lay::RING_OFF) / stage;
+    s = s < 2 ? 2 : (s > kMaxStages ? kMaxStages : s);
+    if (n_stages) *n_stages = s;
+    return (size_t)Lay::RING_OFF + (size_t)s * stage;
+}
+
+size_t rows_bf16_smem_bytes(int head_dim, int k_eq_v, int* n_stages) {
+    switch (head_dim) {
+        case 64: return smem_for<64>(k_eq_v, n_stages);
+        case 128: return smem_for<128>(k_eq_v, n_stages);
+        case 256: return smem_for<256>(k_eq_v, n_stages);
+        case 512: return smem_for<512>(k_eq_v, n_stages);
+    }
+    return 0;
+}
+
+template <int D>
+static cudaError_t launch_bf16_d(const RowsParams& p, dim3 grid, size_t smem, cudaStream_t st) {
+    static bool configured = false;  // attribute set once per process (same value every time)
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(rows_attn_bf16_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             2 * kSmemBudget);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    rows_attn_bf16_kernel<D><<<grid, kRowsThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rows_bf16(const RowsParams& p, int head_dim, dim3 grid, size_t smem,
+                             cudaStream_t st) {
+    switch (head_dim) {
+        case 64: return launch_bf16_d<64>(p, grid, smem, st);
+        case 128: return launch_bf16_d<128>(p, grid, smem, st);
+        case 256: return launch_bf16_d<256>(p, grid, smem, st);
+        case 512: return launch_bf16_d<512>(p, grid, smem, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rows_f32(const RowsParams& p, int head_dim, dim3 grid, cudaStream_t st) {
+    const dim3 block(kF32RowsPerCta * 32);
+    switch (head_dim) {
+        case 64: rows_attn_f32_kernel<64><<<grid, block, 0, st>>>(p); break;
+        case 128: rows_attn_f32_kernel<128><<<grid, block, 0, st>>>(p); break;
+        case 256: rows_attn_f32_kernel<256><<<grid, block, 0, st>>>(p); break;
+        case 512: rows_attn_f32_kernel<512><<<grid, block, 0, st>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out_fp32,
+                           cudaStream_t st) {
+    const dim3 grid(p.n_q, batch);
+    const dim3 block(head_dim / 4 < 32 ? 32 : head_dim / 4);
+    if (out_fp32)
+        combine_kernel<float><<<grid, block, 0, st>>>(p, head_dim);
+    else
+        combine_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(p, head_dim);
+    return cudaGetLastError();
+}
+
+}  // namespace gemma

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every declared symbol;
+argument errors are caught on the host before any CUDA call (runs without a GPU)."""
+import ctypes
+
+import pytest
+
+import mixed_sliding_global_gb300 as g
+from mixed_sliding_global_gb300 import binding
+
+FAKE = 0x10000  # an aligned, never dereferenced stand-in for a device pointer
+
+
+def lib():
+    return g.library()
+
+
+def test_library_exports_every_declared_symbol():
+    names = g.exported_symbols()
+    assert {"gemma_kv_append", "gemma_attn_decode", "gemma_attn_prefill",
+            "gemma_attn_workspace_size", "gemma_status_string", "gemma_abi_version"} <= set(names)
+    raw = ctypes.CDLL(g.library_path())
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings_and_version():
+    assert g.gemma_status_string(0) == "GEMMA_OK"
+    assert g.gemma_status_string(-4) == "GEMMA_ERR_WORKSPACE"
+    assert g.gemma_status_string(99) == "GEMMA_UNKNOWN_STATUS"
+    assert g.gemma_abi_version() == 1
+
+
+def _ptrs(*xs):
+    return (ctypes.c_void_p * len(xs))(*xs)
+
+
+def _i32(*xs):
+    return (ctypes.c_int32 * len(xs))(*xs)
+
+
+def decode(owner=(0,), layer=0, n_layers=None, max_seq_len=64, batch=1, kind=1, window=0, n_q=4,
+           n_kv=1, d=64, k_eq_v=1, cap=64, scale=0.125, dtype=0, ws=None, ws_bytes=0,
+           kc=(FAKE,), vc=(None,)):
+    n_layers = len(owner) if n_layers is None else n_layers
+    return lib().gemma_attn_decode(FAKE, FAKE, _ptrs(*kc), _ptrs(*vc), _i32(*owner), n_layers, layer,
+                                   FAKE, max_seq_len, batch, kind, window, n_q, n_kv, d, k_eq_v,
+                                   cap, scale, dtype, ws, ws_bytes, None, None)
+
+
+INVALID, UNSUPPORTED, CAPACITY = -1, -2, -3
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(owner=(1,)), INVALID),                         # owner after the layer
+    (dict(owner=(0, 0), layer=2), INVALID),              # layer out of range
+    (dict(owner=(0, 0, 1), layer=2, kc=(FAKE, None, None)), INVALID),  # owner that is shared
+    (dict(n_q=6, n_kv=4), INVALID),                      # n_q not a multiple of n_kv
+    (dict(n_q=64, n_kv=2), UNSUPPORTED),                 # group of 32
+    (dict(d=96), UNSUPPORTED),
+    (dict(kind=0, window=0), INVALID),                   # sliding without a window
+    (dict(kind=2), INVALID),
+    (dict(max_seq_len=65), CAPACITY),
+    (dict(max_seq_len=0), INVALID),
+    (dict(k_eq_v=0), INVALID),                           # V cache missing
+    (dict(kc=(None,)), INVALID),
+    (dict(kc=(FAKE + 8,)), INVALID),                     # misaligned cache
+    (dict(dtype=5), INVALID),
+    (dict(scale=float("nan")), INVALID),
+    (dict(batch=-1), INVALID),
+])
+def test_decode_argument_errors(kwargs, status):
+    assert decode(**kwargs) == status
+
+
+def test_empty_batch_is_ok_without_touching_the_device():
+    assert decode(batch=0) == 0
+    assert lib().gemma_attn_prefill(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, 64,
+                                    0, 1, 1, 0, 4, 1, 64, 1, 64, 0.1, 0, None, 0, None, None) == 0
+
+
+def test_append_argument_errors_and_shared_no_op():
+    f = lib().gemma_kv_append
+    # shared layer: OK, nothing to do
+    assert f(_ptrs(FAKE, None), _ptrs(None, None), _i32(0, 0), 2, 1, FAKE, None, FAKE, 1, 1, 1, 64,
+             64, 1, 0, None, None) == 0
+    # n_new beyond capacity
+    assert f(_ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, None, FAKE, 1, 65, 1, 64, 64, 1, 0,
+             None, None) == CAPACITY
+    # V cache missing without k_eq_v
+    assert f(_ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, FAKE, FAKE, 1, 1, 1, 64, 64, 0, 0,
+             None, None) == INVALID
+    assert f(_ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, None, FAKE, 1, 1, 1, 80, 64, 1, 0,
+             None, None) == UNSUPPORTED
+    # empty
+    assert f(_ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, None, FAKE, 0, 1, 1, 64, 64, 1, 0,
+             None, None) == 0
+
+
+def test_workspace_size_rejects_bad_arguments():
+    assert lib().gemma_attn_workspace_size(1, 1, 0, 6, 4, 64, 64, 1) == ctypes.c_size_t(-1).value
+    assert lib().gemma_attn_workspace_size(0, 1, 0, 4, 1, 64, 64, 1) == 0
+    with pytest.raises(ValueError):
+        g.gemma_attn_workspace_size(1, 1, 0, 4, 1, 96, 64, 1)
+
+
+def test_binding_has_no_fallback():
+    # every computing entry point of the binding goes through the shared library
+    src = open(binding.__file__).read()
+    assert "oracle" not in src and "torch.nn.functional" not in src

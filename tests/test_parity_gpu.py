@@ -1,0 +1,170 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, element by element.
+
+Tolerances (stated by the method's target): bf16 outputs with fp32 accumulation must be within
+max |err| <= 2e-2 and mean |err| <= 2e-3 of the oracle; the fp32 debug path within 1e-4.
+Every cache is NaN outside the rows the generator wrote, so any read outside the window or
+past a sequence's length poisons the output and fails the comparison.
+"""
+import pytest
+import torch
+
+import synth
+from synth import GLOBAL, SLIDING, BF16, FP32, LayerSpec, Workload
+from harness import GpuRun, compare, host_inputs, oracle_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_compare(w, layers, seqs=None, q_range=None, max_seq_len=None):
+    hb = host_inputs(w, layers, seqs)
+    ref = oracle_outputs(w, hb, layers, q_range)
+    gr = GpuRun(w, hb)
+    got = {}
+    for l in layers:
+        if w.is_owner(l):
+            gr.append(l)
+        got[l] = gr.attend(l, max_seq_len)
+    torch.cuda.synchronize()
+    assert gr.err.item() == 0, f"device error word {gr.err.item()}"
+    errs = {}
+    for l in layers:
+        g = got[l]
+        if q_range is not None:
+            g = g[:, q_range[0]:q_range[1]]
+        errs[l] = compare(g, ref[l], w.dtype)
+    return errs
+
+
+# ------------------------------------------------------------------------------------------
+# the tiny case, fp32 debug path (<= 1e-4)
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("mode,ctx", [("decode", 64), ("prefill", 64), ("prefill", 72)])
+def test_tiny_fp32(mode, ctx):
+    run_and_compare(synth.tiny(mode, ctx=ctx), [0, 1])
+
+
+def test_tiny_bf16():
+    w = synth.tiny("decode")
+    w.dtype = BF16
+    run_and_compare(w, [0, 1])
+    w = synth.tiny("prefill")
+    w.dtype = BF16
+    run_and_compare(w, [0, 1])
+
+
+# ------------------------------------------------------------------------------------------
+# shape sweep: several tiles, ragged tails, every head_dim and group size, both kinds
+# ------------------------------------------------------------------------------------------
+def one_layer(spec, n_new, ctx_lens, cap, dtype=BF16):
+    return Workload("sweep", [spec], [0], len(ctx_lens), dtype, n_new, list(ctx_lens), cap)
+
+
+DECODE_SHAPES = [
+    # spec, ctx_lens, cap
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), [8192], 8192),
+    (LayerSpec(SLIDING, 1024, 16, 8, 256, False), [8192], 8192),
+    (LayerSpec(SLIDING, 512, 8, 2, 256, False), [2048], 2048),
+    (LayerSpec(GLOBAL, 0, 8, 2, 256, False), [2048], 2048),
+    (LayerSpec(GLOBAL, 0, 4, 4, 64, False), [1, 2, 33, 100, 1000], 1024),
+    (LayerSpec(SLIDING, 37, 8, 1, 128, False), [5, 37, 38, 300], 320),
+    (LayerSpec(GLOBAL, 0, 16, 4, 128, True), [777, 31, 4097], 4160),
+    (LayerSpec(SLIDING, 100, 16, 16, 64, True), [3, 250], 256),
+    (LayerSpec(SLIDING, 1, 2, 1, 256, False), [1, 9], 16),
+    (LayerSpec(GLOBAL, 0, 8, 1, 512, False), [63, 64, 65, 3000], 3008),
+]
+
+
+@pytest.mark.parametrize("case", range(len(DECODE_SHAPES)))
+def test_decode_shapes(case):
+    spec, lens, cap = DECODE_SHAPES[case]
+    run_and_compare(one_layer(spec, 1, lens, cap), [0])
+
+
+@pytest.mark.parametrize("case", [0, 4, 5, 8])
+def test_decode_shapes_fp32(case):
+    spec, lens, cap = DECODE_SHAPES[case]
+    run_and_compare(one_layer(spec, 1, lens, cap, FP32), [0])
+
+
+PREFILL_SHAPES = [
+    # spec, n_new, ctx_lens, cap, q_range
+    (LayerSpec(SLIDING, 7, 4, 2, 64, False), 13, [13, 20, 50], 64, None),
+    (LayerSpec(GLOBAL, 0, 2, 1, 128, True), 9, [9, 100], 128, None),
+    (LayerSpec(SLIDING, 64, 8, 8, 512, False), 33, [40, 200], 200, None),
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 40, [40, 333], 352, None),
+    (LayerSpec(SLIDING, 1024, 16, 8, 256, False), 512, [4096], 4096, (0, 24)),
+    (LayerSpec(SLIDING, 1024, 16, 8, 256, False), 512, [4096], 4096, (488, 512)),
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 512, [4096], 4096, (0, 8)),
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 512, [4096], 4096, (504, 512)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL_SHAPES)))
+def test_prefill_shapes(case):
+    spec, n_new, lens, cap, qr = PREFILL_SHAPES[case]
+    run_and_compare(one_layer(spec, n_new, lens, cap), [0], q_range=qr)
+
+
+@pytest.mark.parametrize("case", [0, 1, 3])
+def test_prefill_shapes_fp32(case):
+    spec, n_new, lens, cap, qr = PREFILL_SHAPES[case]
+    run_and_compare(one_layer(spec, n_new, lens, cap, FP32), [0], q_range=qr)
+
+
+# ------------------------------------------------------------------------------------------
+# the workload configurations at full size
+# ------------------------------------------------------------------------------------------
+def test_e4b_decode_all_layers():
+    """12 layers, 5:1 sliding/global, last four layers KV-shared, batch 1, context 2048."""
+    w = synth.e4b_decode()
+    run_and_compare(w, list(range(w.n_layers)))
+
+
+def test_12b_decode_sliding_and_global():
+    w = synth.b12_decode()
+    run_and_compare(w, [0, 5])
+
+
+def test_ragged_decode_sampled_sequences():
+    """Batch 64 ragged lengths: sequences with the shortest, the longest and two more."""
+    w = synth.ragged_decode(n_layers=6)
+    lens = w.ctx_lens
+    seqs = sorted({lens.index(min(lens)), lens.index(max(lens)), 7, 33})
+    hb_w = Workload(w.name, w.layers, w.owner_map, len(seqs), w.dtype, 1,
+                    [lens[s] for s in seqs], w.capacity)
+    # the sampled sequences keep their own seeded inputs (seeds depend on the sequence index)
+    hb = host_inputs(w, [0, 5], seqs)
+    ref = oracle_outputs(hb_w, hb, [0, 5])
+    gr = GpuRun(hb_w, hb)
+    for l in (0, 5):
+        gr.append(l)
+        got = gr.attend(l, max_seq_len=max(lens))
+        torch.cuda.synchronize()
+        compare(got, ref[l], w.dtype)
+    assert gr.err.item() == 0
+
+
+def test_prefill_bucket_sampled_queries():
+    w = synth.prefill_12b(n_layers=6, batch=2)
+    for qr in ((0, 8), (255, 263), (504, 512)):
+        run_and_compare(w, [0, 5], q_range=qr)
+
+
+# ------------------------------------------------------------------------------------------
+# properties that hold at any size
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("spec", [LayerSpec(GLOBAL, 0, 16, 1, 512, True),
+                                  LayerSpec(SLIDING, 1024, 16, 8, 256, False)])
+def test_split_plan_does_not_change_the_result(spec):
+    """A larger max_seq_len hint changes the split over keys; outputs agree within tolerance."""
+    w = one_layer(spec, 1, [3000, 5000], 16448)
+    hb = host_inputs(w, [0])
+    ref = oracle_outputs(w, hb, [0])[0]
+    outs = []
+    for msl in (5000, 16448):
+        gr = GpuRun(w, hb)
+        gr.append(0)
+        outs.append(gr.attend(0, max_seq_len=msl))
+        torch.cuda.synchronize()
+        compare(outs[-1], ref, BF16)
+    assert (outs[0].float() - outs[1].float()).abs().max().item() <= 2e-2
