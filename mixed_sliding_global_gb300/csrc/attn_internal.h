@@ -40,6 +40,8 @@ cudaError_t launch_rows_bf16(const RowsParams& p, int head_dim, dim3 grid, size_
 cudaError_t launch_rows_f32(const RowsParams& p, int head_dim, dim3 grid, cudaStream_t st);
 cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out_fp32,
                            cudaStream_t st);
+bool prefill_tc_supported(int head_dim);
+cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cudaStream_t st);
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                              const int32_t* write_pos, int batch, int n_new, int n_kv,
                              int capacity, int row_bytes, uint32_t* err, int n_sm,

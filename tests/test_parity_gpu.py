@@ -96,6 +96,12 @@ PREFILL_SHAPES = [
     (LayerSpec(SLIDING, 1024, 16, 8, 256, False), 512, [4096], 4096, (488, 512)),
     (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 512, [4096], 4096, (0, 8)),
     (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 512, [4096], 4096, (504, 512)),
+    # several 128-row tiles on the tensor-memory path (head_dim <= 256)
+    (LayerSpec(GLOBAL, 0, 16, 1, 256, True), 100, [100, 700], 704, None),
+    (LayerSpec(SLIDING, 130, 8, 2, 128, False), 300, [300, 1000], 1024, None),
+    (LayerSpec(GLOBAL, 0, 1, 1, 64, False), 200, [333, 200], 352, None),
+    (LayerSpec(SLIDING, 1024, 16, 8, 256, False), 160, [4096, 1500], 4096, None),
+    (LayerSpec(SLIDING, 5, 4, 4, 256, True), 70, [90, 71], 96, None),
 ]
 
 
