@@ -284,9 +284,11 @@ def build_library(world, local):
     g.library(build_if_missing=False)
 
 
-def workload(name):
+def workload(name, batch=None, layers=None):
     if name == "ragged_decode":
-        return synth.ragged_decode(), [l % RAGGED_PHYS_LAYERS for l in range(48)]
+        nl = layers or 48
+        return (synth.ragged_decode(n_layers=nl, batch=batch or 64),
+                [l % RAGGED_PHYS_LAYERS for l in range(nl)])
     if name == "e4b_decode":
         return synth.e4b_decode(), None
     if name == "12b_decode":
@@ -451,7 +453,7 @@ def run_native(args):
     build_library(world, local)
     device = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    w, phys = workload(args.workload)
+    w, phys = workload(args.workload, args.batch, args.layers)
     decode = w.n_new == 1
     unit = "GB/s" if decode else "TFLOP/s"
     scale = 1e9 if decode else 1e12
@@ -560,6 +562,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="ragged_decode",
                     choices=["ragged_decode", "e4b_decode", "12b_decode", "prefill"])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="smaller ragged batch (profiling captures only; not a bench line)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="fewer ragged layer-steps (profiling captures only; not a bench line)")
     ap.add_argument("--quick", action="store_true",
                     help="main workload only (no e2e, CPU baseline or other configurations)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,

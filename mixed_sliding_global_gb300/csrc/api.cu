@@ -145,7 +145,7 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const long long rows = (long long)n_tok * p.G;
     cudaError_t e;
-    if (dtype == GEMMA_BF16 && n_tok > 1 && gemma::prefill_tc_supported(head_dim) && false) {
+    if (dtype == GEMMA_BF16 && n_tok > 1 && gemma::prefill_tc_supported(head_dim)) {
         e = gemma::launch_prefill_tc(p, head_dim, batch, s);
     } else if (dtype == GEMMA_BF16) {
         const size_t smem = gemma::rows_bf16_smem_bytes(head_dim, p.k_eq_v, &p.n_stages);
