@@ -116,6 +116,30 @@ int gemma_attn_decode(void* out, const void* q, const void* const* k_cache,
                       void* stream);
 
 /*
+ * gemma_attn_decode_static -- gemma_attn_decode without a caller-provided workspace. The pages
+ * have no counterpart: this entry point exists for callers of this library that cannot
+ * allocate device memory (code running inside an allocator or memory-pool callback, a plugin
+ * whose host owns every device allocation, or a latency-critical path that must not call the
+ * driver's allocator). Its split scratch is a fixed 64 MiB array compiled into the library,
+ * held by every GPU that loads the library until the process exits. It allocates nothing.
+ *  - Arguments and results are those of gemma_attn_decode minus workspace/workspace_bytes.
+ *  - Returns GEMMA_ERR_WORKSPACE when gemma_attn_workspace_size(...) for these arguments is
+ *    larger than 64 MiB (e.g. batch 64 x 16 query heads of head_dim 512 split 19 ways needs
+ *    about 40 MB and fits).
+ *  - The first call on each device looks up the array's device address (with that device
+ *    current); make that first call before any stream capture.
+ *  - All calls share the array, which keeps the previous call's contents (nothing in it has to
+ *    start at zero); calls whose kernels overlap on the GPU race on it, so the caller must
+ *    order them (one stream, or events between streams).
+ */
+int gemma_attn_decode_static(void* out, const void* q, const void* const* k_cache,
+                             const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                             int layer, const int32_t* seq_lens, int max_seq_len, int batch,
+                             gemma_layer_kind kind, int window, int n_q, int n_kv, int head_dim,
+                             int k_eq_v, int kv_capacity, float scale, gemma_dtype dtype,
+                             uint32_t* device_error, void* stream);
+
+/*
  * gemma_attn_prefill -- the prefill bucket: n_new query tokens per sequence, written to the
  * cache first (gemma_kv_append), at positions seq_lens[b] - n_new + i, attending causally
  * (and within the window on sliding layers) over the cached prefix and the new tokens.

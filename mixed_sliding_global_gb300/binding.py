@@ -31,6 +31,10 @@ _SIGNATURES = {
                                     _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_void_p,
                                     _c_size_t, _c_void_p, _c_void_p]),
+    "gemma_attn_decode_static": (_c_int, [_c_void_p, _c_void_p, _PVOID, _PVOID, _PI32, _c_int,
+                                          _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_int,
+                                          _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                                          _c_void_p, _c_void_p]),
     "gemma_attn_workspace_size": (_c_size_t, [_c_int] * 8),
     "gemma_status_string": (ctypes.c_char_p, [_c_int]),
     "gemma_abi_version": (_c_int, []),
@@ -194,3 +198,24 @@ def gemma_attn_prefill(out: torch.Tensor, q: torch.Tensor, k_cache, v_cache, own
     _attn("gemma_attn_prefill", out, q, k_cache, v_cache, owner_map, layer, seq_lens, max_seq_len,
           q.shape[1], kind=kind, window=window, n_kv=n_kv, k_eq_v=k_eq_v, scale=scale,
           kv_capacity=kv_capacity, workspace=workspace, device_error=device_error, stream=stream)
+
+
+def gemma_attn_decode_static(out: torch.Tensor, q: torch.Tensor, k_cache, v_cache, owner_map,
+                             layer: int, seq_lens: torch.Tensor, max_seq_len: int, *, kind: int,
+                             window: int, n_kv: int, k_eq_v: bool, scale: float,
+                             kv_capacity: Optional[int] = None,
+                             device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """gemma_attn_decode with the library's built-in scratch instead of a workspace tensor, for
+    callers that cannot allocate device memory (see include/gemma_attn.h)."""
+    B = q.shape[0]
+    n_q, d = q.shape[-2], q.shape[-1]
+    n_layers = len(owner_map)
+    kc = _cache_of(k_cache, owner_map, layer)
+    cap = kv_capacity if kv_capacity is not None else kc.shape[2]
+    vcs = list(v_cache) if v_cache is not None else [None] * n_layers
+    st = library().gemma_attn_decode_static(
+        _dev_ptr(out), _dev_ptr(q), _ptr_array(list(k_cache)), _ptr_array(vcs),
+        _i32_array(owner_map), n_layers, layer, _dev_ptr(seq_lens), int(max_seq_len), B,
+        int(kind), int(window), n_q, int(n_kv), d, int(bool(k_eq_v)), int(cap), float(scale),
+        _dtype(q), _dev_ptr(device_error), _stream(stream))
+    _check("gemma_attn_decode_static", st)
