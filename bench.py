@@ -284,18 +284,30 @@ def build_library(world, local):
     g.library(build_if_missing=False)
 
 
-def workload(name, batch=None, layers=None):
+def _slice(w, offset, nl):
+    """Layers [offset, offset + nl) of a model with its own caches (profiling captures)."""
+    return synth.Workload(w.name, w.layers[offset:offset + nl], list(range(nl)), w.batch, w.dtype,
+                          w.n_new, w.ctx_lens, w.capacity)
+
+
+def workload(name, batch=None, layers=None, offset=0):
     if name == "ragged_decode":
         nl = layers or 48
-        return (synth.ragged_decode(n_layers=nl, batch=batch or 64),
-                [l % RAGGED_PHYS_LAYERS for l in range(nl)])
+        w = synth.ragged_decode(n_layers=offset + nl, batch=batch or 64)
+        if offset:
+            w = _slice(w, offset, nl)
+        return w, [(offset + l) % RAGGED_PHYS_LAYERS for l in range(nl)]
     if name == "e4b_decode":
-        return synth.e4b_decode(), None
-    if name == "12b_decode":
-        return synth.b12_decode(), None
-    if name == "prefill":
-        return synth.prefill_12b(), None
-    raise ValueError(name)
+        w = synth.e4b_decode()
+    elif name == "12b_decode":
+        w = synth.b12_decode()
+    elif name == "prefill":
+        w = synth.prefill_12b(batch=batch or 4)
+    else:
+        raise ValueError(name)
+    if layers or offset:
+        w = _slice(w, offset, layers or (w.n_layers - offset))
+    return w, None
 
 
 def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rotations=1):
@@ -453,7 +465,7 @@ def run_native(args):
     build_library(world, local)
     device = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    w, phys = workload(args.workload, args.batch, args.layers)
+    w, phys = workload(args.workload, args.batch, args.layers, args.layer_offset)
     decode = w.n_new == 1
     unit = "GB/s" if decode else "TFLOP/s"
     scale = 1e9 if decode else 1e12
@@ -478,6 +490,8 @@ def run_native(args):
                 "launch_us": 1e3 * sum(launch_ms) / w.n_layers, "peak_source": peak_src}
         for kind, name in ((synth.SLIDING, "sliding"), (synth.GLOBAL, "global")):
             ls = [l for l, s in enumerate(w.layers) if s.kind == kind]
+            if not ls:
+                continue
             b = sum(per_bytes[l] for l in ls) / len(ls)
             t = sum(launch_ms[l] for l in ls) / len(ls)
             roof[name] = {"bytes_per_launch": b, "launch_us": 1e3 * t,
@@ -489,6 +503,12 @@ def run_native(args):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": None,
                 "kernel": "attention launch (prefill)", "peak_source": peak_src + " sustained"}
+        for kind, name in ((synth.SLIDING, "sliding"), (synth.GLOBAL, "global")):
+            ls = [l for l, s in enumerate(w.layers) if s.kind == kind]
+            if ls:
+                f = sum(per_flops[l] for l in ls)
+                t = sum(launch_ms[l] for l in ls)
+                roof[name] = {"tflops": f / (t * 1e-3) / 1e12, "launch_us": 1e3 * t / len(ls)}
 
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -566,6 +586,8 @@ def main():
                     help="smaller ragged batch (profiling captures only; not a bench line)")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer ragged layer-steps (profiling captures only; not a bench line)")
+    ap.add_argument("--layer-offset", type=int, default=0,
+                    help="first ragged layer (profiling captures only; not a bench line)")
     ap.add_argument("--quick", action="store_true",
                     help="main workload only (no e2e, CPU baseline or other configurations)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,

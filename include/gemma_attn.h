@@ -101,7 +101,8 @@ int gemma_kv_append(void* const* k_cache, void* const* v_cache, const int32_t* o
  *                     layer's kind, n_kv, head_dim and k_eq_v (the caller's contract).
  *   seq_lens          DEVICE int32[batch], 1 <= seq_lens[b] <= max_seq_len.
  *   max_seq_len       HOST bound on seq_lens, used to plan the split over keys.
- *   scale             softmax scale applied to q . k (1/sqrt(head_dim) in the workloads).
+ *   scale             softmax scale applied to q . k, finite and > 0 (1/sqrt(head_dim) in
+ *                     the workloads).
  *   workspace         DEVICE scratch of at least
  *                     gemma_attn_workspace_size(batch, kind, window, n_q, n_kv, head_dim,
  *                     max_seq_len, 1) bytes (may be NULL when that size is 0). Contents on

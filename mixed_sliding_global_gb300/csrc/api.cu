@@ -98,7 +98,8 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     int o = 0;
     st = resolve_owner(owner_map, n_layers, layer, &o);
     if (st != GEMMA_OK) return st;
-    if (kv_capacity < 1 || max_seq_len < n_tok || !std::isfinite(scale)) return GEMMA_ERR_INVALID_ARG;
+    if (kv_capacity < 1 || max_seq_len < n_tok || !std::isfinite(scale) || !(scale > 0.f))
+        return GEMMA_ERR_INVALID_ARG;
     if (max_seq_len > kv_capacity) return GEMMA_ERR_CAPACITY;
     if (batch > 65535) return GEMMA_ERR_UNSUPPORTED;
     if (batch == 0) return GEMMA_OK;

@@ -129,6 +129,13 @@ GEMMA_DEVINL float warp_sum(float v) {
     return v;
 }
 
+// 2^x with the SFU's approximate exp2 (flushes denormal results to zero; -inf gives 0).
+GEMMA_DEVINL float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 GEMMA_DEVINL uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

@@ -6,7 +6,7 @@
 // owner layer ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", sections 2.1-2.3; the
 // pages' "eager" matmul-softmax-matmul definition, section 4.3).
 //
-// One CTA per (128-row tile, KV head, sequence); 6 warps:
+// Each CTA has 6 warps:
 //   warps 0-3  softmax: thread r owns row r (TMEM lane r): loads its Q row into TMEM, reads
 //              its S row from TMEM, masks by index, keeps (m, l), writes bf16 P to shared
 //              memory, rescales its O row in TMEM when the running max grows by more than
@@ -17,7 +17,16 @@
 //   warp 5     MMA issuer: S = Q K^T (A = Q from TMEM, B = K, K-major) and O += P V (A = P,
 //              K-major, B = V, MN-major), fp32 accumulation in TMEM; tcgen05.commit signals
 //              the mbarriers that order the warps.
-// TMEM (512 columns): Q (head_dim/2 columns of packed bf16), S (128), O (head_dim).
+// TMEM (512 columns): Q (DH/2 columns of packed bf16), S (128), O (DH), DH = head_dim / CL.
+//
+// CL = 2 (head_dim 512): a 128 x 512 fp32 O alone would fill the 512 TMEM columns of an SM,
+// so a cluster of two CTAs splits head_dim: CTA h holds Q[:, 256h:256h+256] and reads only
+// that half of K and V. Each computes a partial S over its half, sends it to its peer through
+// distributed shared memory (fp32), and adds the peer's partial to its own: both CTAs obtain
+// bit-identical S (IEEE addition commutes), hence identical P, m and l, and each accumulates
+// and writes its own half of O. No multiply-add is done twice. With k_eq_v the K half is also
+// the V half.
+//
 // The key range of the tile is clamped to [first row's window start, last row's position]
 // before any load; rows of the last partial key tile beyond the range are zeroed in shared
 // memory before they enter P V.
@@ -36,25 +45,76 @@ constexpr float kLazyRescaleLog2 = 8.f;
 struct TcParams {
     RowsParams p;
     int n_slots;
-    int slot_bytes;
 };
 
-template <int D>
+template <int D, int CL>
 struct TcLayout {
-    static constexpr int CHUNKS = D / 64;              // 64-column boxes per K/V tile
+    static constexpr int DH = D / CL;                    // head_dim columns owned by a CTA
+    static constexpr int CHUNKS = DH / 64;               // 64-column boxes per K/V tile
     static constexpr int SLOT = CHUNKS * kTcKeys * 128;  // bytes of one K or V tile
-    static constexpr int P_BYTES = kTcKeys * 128 * 2;   // 128 rows x 128 keys bf16
-    static constexpr int Q_COL = 0;                       // TMEM columns
+    static constexpr int P_BYTES = kTcKeys * 128 * 2;    // 128 rows x 128 keys bf16
+    static constexpr int X_BYTES = CL > 1 ? 128 * kTcKeys * 4 : 0;  // peer's partial S (fp32)
+    static constexpr int Q_COL = 0;                      // TMEM columns
     static constexpr int S_COL = 128;
     static constexpr int O_COL = 256;
-    static_assert(D / 2 <= 128 && 256 + D <= 512, "TMEM budget");
+    static_assert(DH / 2 <= 128 && 256 + DH <= 512, "TMEM budget");
 };
 
-template <int D>
+// ---------------------------------------------------------------------------------------------
+// cluster helpers (distributed shared memory between the two CTAs of a cluster)
+// ---------------------------------------------------------------------------------------------
+GEMMA_DEVINL uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+GEMMA_DEVINL void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+GEMMA_DEVINL uint32_t map_to_peer(const void* local, uint32_t peer) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(peer));
+    return r;
+}
+GEMMA_DEVINL void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+GEMMA_DEVINL void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+GEMMA_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (data written by the peer CTA becomes visible).
+GEMMA_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* err) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+            report(err, GEMMA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+template <int D, int CL>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const TcParams tp) {
-    using Lay = TcLayout<D>;
+    using Lay = TcLayout<D, CL>;
+    constexpr int DH = Lay::DH;
     const RowsParams& p = tp.p;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -62,7 +122,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int NS = tp.n_slots;
     uint8_t* slots = smem;
     uint8_t* sP = smem + NS * Lay::SLOT;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + Lay::P_BYTES);
+    float* sX = reinterpret_cast<float*>(sP + Lay::P_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + Lay::P_BYTES + Lay::X_BYTES);
     uint64_t* kv_full = bars;
     uint64_t* kv_empty = bars + kTcMaxSlots;
     uint64_t* q_ready = bars + 2 * kTcMaxSlots;
@@ -70,10 +131,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* s_free = q_ready + 2;
     uint64_t* p_full = q_ready + 3;
     uint64_t* o_done = q_ready + 4;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(q_ready + 5);
+    uint64_t* x_full = q_ready + 5;  // the peer's partial S has landed in sX
+    uint64_t* x_free = q_ready + 6;  // the peer has read the partial S this CTA sent it
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(q_ready + 7);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const uint32_t h = CL > 1 ? cluster_rank() : 0u;  // which head_dim part this CTA owns
+    const int rt = blockIdx.x / CL, kvh = blockIdx.y, b = blockIdx.z;
     const int rows_total = p.n_tok * p.G;
     const int row0 = rt * 128;
     const int n_rows = min(128, rows_total - row0);
@@ -103,10 +167,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(s_free, 4);
         mbar_init(p_full, 4);
         mbar_init(o_done, 1);
+        mbar_init(x_full, 128);
+        mbar_init(x_free, 128);
         fence_barrier_init();
     }
     tc_fence_before();
     __syncthreads();
+    if (CL > 1) cluster_sync();  // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tQ = tmem + Lay::Q_COL, tS = tmem + Lay::S_COL, tO = tmem + Lay::O_COL;
@@ -124,14 +191,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint8_t* dst = slots + s * Lay::SLOT;
                 mbar_arrive_expect_tx(&kv_full[s], Lay::SLOT);
                 for (int c = 0; c < Lay::CHUNKS; ++c)
-                    tma_load_3d(dst + c * kTcKeys * 128, map, c * 64, k_begin + t * kTcKeys, row3,
-                                &kv_full[s]);
+                    tma_load_3d(dst + c * kTcKeys * 128, map, (int)h * DH + c * 64,
+                                k_begin + t * kTcKeys, row3, &kv_full[s]);
             }
         }
     } else if (warp == 5) {
         // -------------------------------- MMA issuer ---------------------------------------
         const uint32_t id_qk = idesc_bf16(128, kTcKeys, 0, 0);
-        const uint32_t id_pv = idesc_bf16(128, D, 0, 1);
+        const uint32_t id_pv = idesc_bf16(128, DH, 0, 1);
         bool ok = mbar_wait(q_ready, 0, p.err);
         auto zero_tail = [&](uint8_t* tile, int n_valid) {
             // rows [n_valid, 128) of every 64-column box: whole 128-byte rows, so the
@@ -211,13 +278,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
             hi = pos + 1;
         }
-        // Q row into TMEM (zeros for rows outside the tile)
+        // this CTA's part of the Q row into TMEM (zeros for rows outside the tile)
         {
             const uint4* qrow = reinterpret_cast<const uint4*>(
                 reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                (((size_t)b * p.n_tok + token) * p.n_q + head) * (size_t)D);
+                (((size_t)b * p.n_tok + token) * p.n_q + head) * (size_t)D + h * DH);
 #pragma unroll
-            for (int j = 0; j < D / 64; ++j) {
+            for (int j = 0; j < DH / 64; ++j) {
                 uint32_t v[32];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -233,6 +300,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(q_ready);
+
+        uint32_t peer_x = 0, peer_x_full = 0, peer_x_free = 0;
+        if (CL > 1) {
+            peer_x = map_to_peer(sX + r * kTcKeys, h ^ 1u);
+            peer_x_full = map_to_peer(x_full, h ^ 1u);
+            peer_x_free = map_to_peer(x_free, h ^ 1u);
+        }
 
         bool ok = true;
         float m_ref = -INFINITY, l = 0.f;
@@ -252,16 +326,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
 
+            if (CL > 1) {
+                // send this row's partial scores to the peer, then add the peer's partial
+                if (t >= 1 && ok) ok = mbar_wait_cluster(x_free, (t - 1) & 1, p.err);
+                // 16-byte chunk c of row r sits at chunk c ^ (r & 7): rows r..r+7 of a warp
+                // phase then fall in different banks on both the remote store and local load
+#pragma unroll
+                for (int c = 0; c < kTcKeys / 4; ++c)
+                    st_cluster_v4(peer_x + ((c ^ (r & 7)) * 16), s[4 * c], s[4 * c + 1],
+                                  s[4 * c + 2], s[4 * c + 3]);
+                mbar_arrive_remote(peer_x_full);
+                if (ok) ok = mbar_wait_cluster(x_full, t & 1, p.err);
+                const float4* xr = reinterpret_cast<const float4*>(sX + r * kTcKeys);
+#pragma unroll
+                for (int e = 0; e < kTcKeys / 4; ++e) {
+                    const float4 x = xr[e ^ (r & 7)];
+                    s[4 * e + 0] += x.x;
+                    s[4 * e + 1] += x.y;
+                    s[4 * e + 2] += x.z;
+                    s[4 * e + 3] += x.w;
+                }
+                mbar_arrive_remote(peer_x_free);
+            }
+
+            // scores stay raw; scale > 0, so max(raw) * scale_log2 is the max of scaled scores
             const int kt0 = k_begin + t * kTcKeys;
             const bool full = kt0 >= lo && kt0 + kTcKeys <= hi;
-            float mx = -INFINITY;
+            if (!full) {
 #pragma unroll
-            for (int e = 0; e < kTcKeys; ++e) {
-                const int key = kt0 + e;
-                const bool valid = full || (key >= lo && key < hi);
-                s[e] = valid ? s[e] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[e]);
+                for (int e = 0; e < kTcKeys; ++e) {
+                    const int key = kt0 + e;
+                    if (key < lo || key >= hi) s[e] = -INFINITY;
+                }
             }
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+            for (int e = 8; e < kTcKeys; e += 8)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[e + i]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                             p.scale_log2;
             const bool need = mx > m_ref + kLazyRescaleLog2;
             const float m_new = need ? mx : m_ref;
             if (t > 0 && ok) ok = mbar_wait(o_done, (t - 1) & 1, p.err);
@@ -269,7 +376,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float alpha = need ? exp2f(m_ref - m_new) : 1.f;
                 tc_fence_after();
 #pragma unroll 1
-                for (int j = 0; j < D / 32; ++j) {
+                for (int j = 0; j < DH / 32; ++j) {
                     uint32_t v[32];
                     tmem_ld32(tO + lane_off + j * 32, v);
                     tmem_ld_wait();
@@ -281,8 +388,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 l *= alpha;
             }
             m_ref = m_new;
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            float sum = 0.f;
+            // p = 2^(raw * scale_log2 - m): one FFMA and one MUFU exp2 per score
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
@@ -291,23 +399,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int k0 = kb * 64 + c * 8 + 2 * e;
-                        const __nv_bfloat162 pr = __floats2bfloat162_rn(exp2f(s[k0] - m_use),
-                                                                         exp2f(s[k0 + 1] - m_use));
-                        const float2 back = __bfloat1622float2(pr);
-                        sum += back.x + back.y;
-                        w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+                        const float p0 = fast_exp2(fmaf(s[k0], p.scale_log2, neg_m));
+                        const float p1 = fast_exp2(fmaf(s[k0 + 1], p.scale_log2, neg_m));
+                        sum4[e] += p0 + p1;
+                        w[e] = pack_bf16(p0, p1);
                     }
                     *reinterpret_cast<uint4*>(sP + kb * (kTcKeys * 128) + r * 128 +
                                               ((c ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-            l += sum;
+            l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
 
-        // epilogue: O / l -> bf16 rows of out (zeros for a sequence with a bad length)
+        // epilogue: O / l -> bf16 (zeros for a sequence with a bad length)
         if (n_tiles > 0 && ok) ok = mbar_wait(o_done, (n_tiles - 1) & 1, p.err);
         tc_fence_after();
         {
@@ -315,10 +422,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int R = row0 + (r < n_rows ? r : 0);
             const int tk = R / p.G, hd = kvh * p.G + (R - tk * p.G);
             uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                                   (((size_t)b * p.n_tok + tk) * p.n_q + hd) * (size_t)D);
+                                                   (((size_t)b * p.n_tok + tk) * p.n_q + hd) * (size_t)D +
+                                                   h * DH);
             const float inv = (bad || l == 0.f) ? 0.f : 1.f / l;
 #pragma unroll 1
-            for (int j = 0; j < D / 32; ++j) {
+            for (int j = 0; j < DH / 32; ++j) {
                 uint32_t v[32];
                 if (n_tiles > 0) {
                     tmem_ld32(tO + lane_off + j * 32, v);
@@ -338,10 +446,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         }
-        if (bad && r == 0 && kvh == 0 && rt == 0) report(p.err, GEMMA_DEVERR_SEQ_LEN);
+        if (bad && r == 0 && kvh == 0 && rt == 0 && h == 0) report(p.err, GEMMA_DEVERR_SEQ_LEN);
     }
     tc_fence_before();
     __syncthreads();
+    if (CL > 1) cluster_sync();  // the peer no longer writes into this CTA's shared memory
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -349,9 +458,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, int CL>
 static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
-    using Lay = TcLayout<D>;
+    using Lay = TcLayout<D, CL>;
     CUtensorMap km, vm;
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.cap, (uint64_t)batch * p.n_kv};
     const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.cap * D * 2};
@@ -360,34 +469,47 @@ static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
     if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
     TcParams tp;
     tp.p = p;
-    tp.slot_bytes = Lay::SLOT;
-    const int fixed = Lay::P_BYTES + 256 + 1024;  // P, barriers, alignment slack
+    const int fixed = Lay::P_BYTES + Lay::X_BYTES + 256 + 1024;  // P, X, barriers, alignment
     int ns = (kTcSmemLimit - fixed) / Lay::SLOT;
     if (ns > kTcMaxSlots) ns = kTcMaxSlots;
+    if (ns < 2) return cudaErrorInvalidValue;
     tp.n_slots = ns;
     const size_t smem = (size_t)ns * Lay::SLOT + fixed;
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemLimit);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
     const int rows = p.n_tok * p.G;
-    dim3 grid((rows + 127) / 128, p.n_kv, batch);
-    prefill_tc_kernel<D><<<grid, kTcThreads, smem, st>>>(km, vm, tp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL * ((rows + 127) / 128), p.n_kv, batch);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL>, km, vm, tp);
 }
 
-bool prefill_tc_supported(int head_dim) { return head_dim == 64 || head_dim == 128 || head_dim == 256; }
+bool prefill_tc_supported(int head_dim) {
+    return head_dim == 64 || head_dim == 128 || head_dim == 256 || head_dim == 512;
+}
 
 cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cudaStream_t st) {
     switch (head_dim) {
-        case 64: return launch_d<64>(p, batch, st);
-        case 128: return launch_d<128>(p, batch, st);
-        case 256: return launch_d<256>(p, batch, st);
+        case 64: return launch_d<64, 1>(p, batch, st);
+        case 128: return launch_d<128, 1>(p, batch, st);
+        case 256: return launch_d<256, 1>(p, batch, st);
+        case 512: return launch_d<512, 2>(p, batch, st);
     }
     return cudaErrorInvalidValue;
 }

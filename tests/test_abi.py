@@ -66,6 +66,8 @@ INVALID, UNSUPPORTED, CAPACITY = -1, -2, -3
     (dict(kc=(FAKE + 8,)), INVALID),                     # misaligned cache
     (dict(dtype=5), INVALID),
     (dict(scale=float("nan")), INVALID),
+    (dict(scale=0.0), INVALID),
+    (dict(scale=-0.5), INVALID),
     (dict(batch=-1), INVALID),
 ])
 def test_decode_argument_errors(kwargs, status):
