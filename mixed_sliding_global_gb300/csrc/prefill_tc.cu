@@ -150,8 +150,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int k_begin = p.is_sliding ? max(0, pos_first - p.window + 1) : 0;
     const int k_end = pos_last + 1;
     const int n_tiles = bad ? 0 : (k_end - k_begin + kTcKeys - 1) / kTcKeys;
-    const int ops_per_tile = p.k_eq_v ? 1 : 2;
-    const int n_ops = n_tiles * ops_per_tile;
+    // K/V ring split: with K = V one ring of NS slots; otherwise NV slots for V (V is needed
+    // only by P V, which comes last) and the rest for K
+    const int NV = p.k_eq_v ? 0 : (NS / 3 > 1 ? NS / 3 : 1);
+    const int NK = NS - NV;
 
     if (warp == 5) {
         tmem_alloc(tslot, 512);
@@ -180,19 +182,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 4) {
         // ------------------------------- TMA producer --------------------------------------
+        // K tiles use slots [0, NK), V tiles slots [NK, NS). K runs one tile ahead of V, so a
+        // K slot is refilled as soon as its S = Q K^T finished, independently of P V.
         if (lane == 0) {
             const int row3 = b * p.n_kv + kvh;
-            for (int u = 0; u < n_ops; ++u) {
-                const int s = u % NS;
-                if (u >= NS && !mbar_wait(&kv_empty[s], ((u / NS) - 1) & 1, p.err)) break;
-                const int t = u / ops_per_tile;
-                const bool is_v = (u % ops_per_tile) == 1;
-                const CUtensorMap* map = is_v ? &vmap : &kmap;
-                uint8_t* dst = slots + s * Lay::SLOT;
-                mbar_arrive_expect_tx(&kv_full[s], Lay::SLOT);
+            auto load = [&](const CUtensorMap* map, int slot, int t) {
+                uint8_t* dst = slots + slot * Lay::SLOT;
+                mbar_arrive_expect_tx(&kv_full[slot], Lay::SLOT);
                 for (int c = 0; c < Lay::CHUNKS; ++c)
                     tma_load_3d(dst + c * kTcKeys * 128, map, (int)h * DH + c * 64,
-                                k_begin + t * kTcKeys, row3, &kv_full[s]);
+                                k_begin + t * kTcKeys, row3, &kv_full[slot]);
+            };
+            bool ok = true;
+            for (int i = 0; i <= n_tiles && ok; ++i) {
+                const int tk = i;          // K tile issued at step i
+                const int tv = i - 1;      // V tile issued at step i
+                if (tk < n_tiles) {
+                    const int sl = tk % NK;
+                    if (tk >= NK) ok = mbar_wait(&kv_empty[sl], ((tk / NK) - 1) & 1, p.err);
+                    if (ok) load(&kmap, sl, tk);
+                }
+                if (!p.k_eq_v && tv >= 0 && ok) {
+                    const int sl = NK + tv % NV;
+                    if (tv >= NV) ok = mbar_wait(&kv_empty[sl], ((tv / NV) - 1) & 1, p.err);
+                    if (ok) load(&vmap, sl, tv);
+                }
             }
         }
     } else if (warp == 5) {
@@ -215,10 +229,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         auto issue_pv = [&](int j) {
             if (ok) ok = mbar_wait(p_full, j & 1, p.err);
-            const int uv = j * ops_per_tile + ops_per_tile - 1;
-            const int sv = uv % NS;
+            const int sv = p.k_eq_v ? j % NK : NK + j % NV;
             if (ok && !p.k_eq_v) {
-                ok = mbar_wait(&kv_full[sv], (uv / NS) & 1, p.err);
+                ok = mbar_wait(&kv_full[sv], (j / NV) & 1, p.err);
                 const int n_valid = k_end - (k_begin + j * kTcKeys);
                 if (n_valid < kTcKeys) zero_tail(slots + sv * Lay::SLOT, n_valid);
             }
@@ -239,9 +252,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
         };
         for (int t = 0; t < n_tiles; ++t) {
-            const int uk = t * ops_per_tile;
-            const int sk = uk % NS;
-            if (ok) ok = mbar_wait(&kv_full[sk], (uk / NS) & 1, p.err);
+            const int sk = t % NK;
+            if (ok) ok = mbar_wait(&kv_full[sk], (t / NK) & 1, p.err);
             if (p.k_eq_v) {
                 const int n_valid = k_end - (k_begin + t * kTcKeys);
                 if (n_valid < kTcKeys) zero_tail(slots + sk * Lay::SLOT, n_valid);
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         uint32_t peer_x = 0, peer_x_full = 0, peer_x_free = 0;
         if (CL > 1) {
-            peer_x = map_to_peer(sX + r * kTcKeys, h ^ 1u);
+            peer_x = map_to_peer(sX + 4 * r, h ^ 1u);
             peer_x_full = map_to_peer(x_full, h ^ 1u);
             peer_x_free = map_to_peer(x_free, h ^ 1u);
         }
@@ -329,18 +341,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (CL > 1) {
                 // send this row's partial scores to the peer, then add the peer's partial
                 if (t >= 1 && ok) ok = mbar_wait_cluster(x_free, (t - 1) & 1, p.err);
-                // 16-byte chunk c of row r sits at chunk c ^ (r & 7): rows r..r+7 of a warp
-                // phase then fall in different banks on both the remote store and local load
+                // chunk-major layout X[c][r] (16-byte chunks): a warp's 32 stores of chunk c
+                // are one contiguous 512-byte write, and the local loads are contiguous too
 #pragma unroll
                 for (int c = 0; c < kTcKeys / 4; ++c)
-                    st_cluster_v4(peer_x + ((c ^ (r & 7)) * 16), s[4 * c], s[4 * c + 1],
-                                  s[4 * c + 2], s[4 * c + 3]);
+                    st_cluster_v4(peer_x + c * (128 * 16), s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                                  s[4 * c + 3]);
                 mbar_arrive_remote(peer_x_full);
                 if (ok) ok = mbar_wait_cluster(x_full, t & 1, p.err);
-                const float4* xr = reinterpret_cast<const float4*>(sX + r * kTcKeys);
+                const float4* xr = reinterpret_cast<const float4*>(sX) + r;
 #pragma unroll
                 for (int e = 0; e < kTcKeys / 4; ++e) {
-                    const float4 x = xr[e ^ (r & 7)];
+                    const float4 x = xr[e * 128];
                     s[4 * e + 0] += x.x;
                     s[4 * e + 1] += x.y;
                     s[4 * e + 2] += x.z;
