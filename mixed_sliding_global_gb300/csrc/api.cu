@@ -12,7 +12,14 @@ using gemma::RowsParams;
 namespace {
 
 constexpr int kMaxSplit = 128;
-constexpr int kMinChunkKeys = 256;  // keys per split chunk when work is plentiful
+#ifndef GEMMA_MIN_CHUNK_KEYS
+#define GEMMA_MIN_CHUNK_KEYS 256
+#endif
+#ifndef GEMMA_SPLIT_CTAS_PER_SM
+#define GEMMA_SPLIT_CTAS_PER_SM 8
+#endif
+constexpr int kMinChunkKeys = GEMMA_MIN_CHUNK_KEYS;  // keys per split chunk when work is plentiful
+constexpr long long kSplitCtasPerSm = GEMMA_SPLIT_CTAS_PER_SM;
 
 int sm_count() {
     static int cache[64] = {0};
@@ -69,7 +76,8 @@ Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim,
     const long long n_read = kind == GEMMA_SLIDING && window < max_seq_len ? window : max_seq_len;
     const long long total = (long long)batch * n_kv * n_read;
     const long long one_per_sm = round_up((total + n_sm - 1) / n_sm, T);
-    const long long eight_per_sm = round_up((total + 8LL * n_sm - 1) / (8LL * n_sm), T);
+    const long long eight_per_sm =
+        round_up((total + kSplitCtasPerSm * n_sm - 1) / (kSplitCtasPerSm * n_sm), T);
     long long chunk = one_per_sm < kMinChunkKeys ? one_per_sm : kMinChunkKeys;
     if (eight_per_sm > chunk) chunk = eight_per_sm;
     if (chunk < T) chunk = T;

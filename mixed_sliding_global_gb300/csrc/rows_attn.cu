@@ -10,28 +10,39 @@
 // bf16 kernel design (per CTA: one KV head of one sequence, 16 query rows, one key chunk):
 //  - the key range is clamped to the window / causal limit before any load (no predicated
 //    loads of keys the tile cannot attend);
-//  - a producer warp streams 32-key K/V tiles with TMA bulk copies (one per cache row, so
-//    only the rows in range are read) into a shared-memory ring with padded rows, so the
-//    ldmatrix reads below are bank-conflict free; every K/V tile is read from HBM once and
-//    reused by all rows (all query heads of the GQA group, and all tokens of the tile);
+//  - a producer warp streams 32-key K/V tiles with tiled TMA (one box per 64 columns of
+//    head_dim, 128-byte swizzle) into a shared-memory ring; the ldmatrix reads below apply
+//    the same swizzle, so they are bank-conflict free; every K/V tile is read from HBM once
+//    and reused by all rows (all query heads of the GQA group, and all tokens of the tile);
+//    rows past the chunk's last key are loaded but masked (scores) and zeroed (values) in
+//    registers;
 //  - eight consumer warps: (1) S = Q K^T with mma.sync m16n8k16 (warps split keys x head_dim),
 //    (2) per-row online softmax in exp2 form with warp shuffles, P rounded to bf16,
 //    (3) O = diag(alpha) O + P V (warps split head_dim);
 //  - fp32 accumulation throughout; partial (m, l, O) per chunk when the keys are split.
 #include "attn_internal.h"
 #include "common.cuh"
+#include "tc.cuh"
+#include "tmap.h"
 
 namespace gemma {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kRowsThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 8;
-constexpr int kSmemBudget = 113 * 1024;  // two CTAs per SM
+#ifndef GEMMA_ROWS_SMEM_BUDGET
+#define GEMMA_ROWS_SMEM_BUDGET (113 * 1024)  // two CTAs per SM
+#endif
+#ifndef GEMMA_ROWS_MIN_BLOCKS
+#define GEMMA_ROWS_MIN_BLOCKS 2
+#endif
+constexpr int kSmemBudget = GEMMA_ROWS_SMEM_BUDGET;
 
 template <int D>
 struct RowsLayout {
-    static constexpr int ROW = 2 * D + 16;  // padded bytes per cache row in shared memory
-    static constexpr int TILE = kKeyTile * ROW;
+    static constexpr int ROW = 2 * D + 16;      // padded bytes per Q row in shared memory
+    static constexpr int BOX = kKeyTile * 128;  // one TMA box: 32 keys x 64 columns (swizzled)
+    static constexpr int TILE = (D / 64) * BOX; // one K or V tile
     static constexpr int KSPLIT = D >= 512 ? 4 : 2;  // warps sharing one n-tile in S = QK^T
     static constexpr int S_STRIDE = kKeyTile + 8;    // fp32 words per S row
     static constexpr int P_STRIDE = kKeyTile + 8;    // bf16 elements per P row
@@ -40,8 +51,16 @@ struct RowsLayout {
     static constexpr int P_OFF = S_OFF + KSPLIT * kRowTile * S_STRIDE * 4;
     static constexpr int STAT_OFF = P_OFF + kRowTile * P_STRIDE * 2;  // alpha, m, l [16] each
     static constexpr int BAR_OFF = (STAT_OFF + 3 * kRowTile * 4 + 15) / 16 * 16;
-    static constexpr int RING_OFF = (BAR_OFF + 2 * kMaxStages * 8 + 127) / 128 * 128;
+    static constexpr int RING_OFF = (BAR_OFF + 2 * kMaxStages * 8 + 1023) / 1024 * 1024;
 };
+
+// Byte offset of element (key, d) in a K/V tile written by TMA with 128-byte swizzle: box
+// d / 64, 128-byte row `key`, 16-byte chunk ((d / 8) % 8) ^ (key % 8).
+template <int D>
+GEMMA_DEVINL uint32_t tile_off(int key, int d) {
+    return (uint32_t)((d >> 6) * RowsLayout<D>::BOX + key * 128 +
+                      ((((d >> 3) & 7) ^ (key & 7)) << 4) + (d & 7) * 2);
+}
 
 // Row geometry: local row r of tile rt is global row R = rt*16 + r, token R / G, member R % G.
 struct RowInfo {
@@ -72,7 +91,9 @@ GEMMA_DEVINL void zero_rows(const RowsParams& p, int b, int kvh, int row0, int n
 }
 
 template <int D>
-__global__ void __launch_bounds__(kRowsThreads, 2) rows_attn_bf16_kernel(const RowsParams p) {
+__global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
+    rows_attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
+                          const __grid_constant__ CUtensorMap vmap, const RowsParams p) {
     using Lay = RowsLayout<D>;
     constexpr int T = kKeyTile;
     constexpr int KSPLIT = Lay::KSPLIT;
@@ -82,7 +103,9 @@ __global__ void __launch_bounds__(kRowsThreads, 2) rows_attn_bf16_kernel(const R
     constexpr int NB = D / 8 / 8;                     // 8-column n-tiles per warp in O
     static_assert(KS % 2 == 0 && NTW >= 1, "tile shape");
 
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x % p.n_split;
     const int rt = blockIdx.x / p.n_split;
@@ -151,21 +174,21 @@ __global__ void __launch_bounds__(kRowsThreads, 2) rows_attn_bf16_kernel(const R
     __syncthreads();
 
     if (warp == kConsumerWarps) {
-        // ---------------- producer warp: TMA bulk copies of the K/V rows in range ----------------
-        const size_t head_base = ((size_t)b * p.n_kv + kvh) * (size_t)p.cap + (size_t)kb;
-        const uint8_t* kg = reinterpret_cast<const uint8_t*>(p.k) + head_base * (2 * D);
-        const uint8_t* vg = reinterpret_cast<const uint8_t*>(p.v) + head_base * (2 * D);
-        for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % S;
-            if (t >= S && !mbar_wait(&empty[s], ((t / S) - 1) & 1, p.err)) break;
-            const int rows = min(T, n_keys - t * T);
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(rows * 2 * D * nops));
-            __syncwarp();
-            uint8_t* dk = ring + s * stage_bytes;
-            for (int r = lane; r < rows; r += 32) {
-                const size_t off = (size_t)(t * T + r) * (2 * D);
-                bulk_g2s(dk + r * Lay::ROW, kg + off, 2 * D, &full[s]);
-                if (nops == 2) bulk_g2s(dk + Lay::TILE + r * Lay::ROW, vg + off, 2 * D, &full[s]);
+        // ---------------- producer warp: tiled TMA loads of the K/V rows in range --------------
+        if (lane == 0) {
+            const int row3 = b * p.n_kv + kvh;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int s = t % S;
+                if (t >= S && !mbar_wait(&empty[s], ((t / S) - 1) & 1, p.err)) break;
+                uint8_t* dk = ring + s * stage_bytes;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_3d(dk + c * Lay::BOX, &kmap, c * 64, kb + t * T, row3, &full[s]);
+                    if (nops == 2)
+                        tma_load_3d(dk + Lay::TILE + c * Lay::BOX, &vmap, c * 64, kb + t * T, row3,
+                                    &full[s]);
+                }
             }
         }
         return;
@@ -226,8 +249,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2) rows_attn_bf16_kernel(const R
                 for (int j = 0; j < NTW; ++j) {
                     const int key = (ng * NTW + j) * 8 + (lane & 7);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(smem_u32(tK + key * Lay::ROW + (d0 + (lane >> 3) * 8) * 2), b0, b1, b2,
-                            b3);
+                    ldsm_x4(smem_u32(tK + tile_off<D>(key, d0 + (lane >> 3) * 8)), b0, b1, b2, b3);
                     mma_bf16(sacc[j], qa[2 * ks2][0], qa[2 * ks2][1], qa[2 * ks2][2],
                              qa[2 * ks2][3], b0, b1);
                     mma_bf16(sacc[j], qa[2 * ks2 + 1][0], qa[2 * ks2 + 1][1], qa[2 * ks2 + 1][2],
@@ -299,7 +321,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2) rows_attn_bf16_kernel(const R
                     const int col = warp * (D / 8) + j * 8 + (lane >> 4) * 8;
                     if (j + 1 < NB) {
                         uint32_t v0, v1, v2, v3;
-                        ldsm_x4_t(smem_u32(tV + vkey * Lay::ROW + col * 2), v0, v1, v2, v3);
+                        ldsm_x4_t(smem_u32(tV + tile_off<D>(vkey, col)), v0, v1, v2, v3);
                         mma_bf16(o[j], pa0, pa1, pa2, pa3, v0 & mlo, v1 & mhi);
                         mma_bf16(o[j + 1], pa0, pa1, pa2, pa3, v2 & mlo, v3 & mhi);
                     } else {
@@ -308,7 +330,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2) rows_attn_bf16_kernel(const R
                         asm volatile(
                             "ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
                             : "=r"(v0), "=r"(v1)
-                            : "r"(smem_u32(tV + vkey * Lay::ROW + c1 * 2)));
+                            : "r"(smem_u32(tV + tile_off<D>(vkey, c1))));
                         mma_bf16(o[j], pa0, pa1, pa2, pa3, v0 & mlo, v1 & mhi);
                     }
                 }
@@ -480,10 +502,11 @@ template <int D>
 static size_t smem_for(int k_eq_v, int* n_stages) {
     using Lay = RowsLayout<D>;
     const int stage = (k_eq_v ? 1 : 2) * Lay::TILE;
-    int s = (kSmemBudget - Lay::RING_OFF) / stage;
+    const int fixed = Lay::RING_OFF + 1024;  // + alignment slack of the dynamic buffer
+    int s = (kSmemBudget - fixed) / stage;
     s = s < 2 ? 2 : (s > kMaxStages ? kMaxStages : s);
     if (n_stages) *n_stages = s;
-    return (size_t)Lay::RING_OFF + (size_t)s * stage;
+    return (size_t)fixed + (size_t)s * stage;
 }
 
 size_t rows_bf16_smem_bytes(int head_dim, int k_eq_v, int* n_stages) {
@@ -502,11 +525,17 @@ static cudaError_t launch_bf16_d(const RowsParams& p, dim3 grid, size_t smem, cu
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(rows_attn_bf16_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             2 * kSmemBudget);
+                                             227 * 1024);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    rows_attn_bf16_kernel<D><<<grid, kRowsThreads, smem, st>>>(p);
+    CUtensorMap km, vm;
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.cap, (uint64_t)grid.z * p.n_kv};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.cap * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)kKeyTile, 1};
+    if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    rows_attn_bf16_kernel<D><<<grid, kRowsThreads, smem, st>>>(km, vm, p);
     return cudaGetLastError();
 }
 
