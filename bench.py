@@ -39,9 +39,11 @@ METRIC = "decode-attn HBM GB/s (% of 8 TB/s); prefill-attn bf16 TFLOP/s (% of pe
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 RAGGED_PHYS_LAYERS = 6   # distinct caches for 48 ragged layer-steps (one 5:1 period)
 
-# dram bytes per algorithmic byte of the decode row kernel from the committed ncu capture
-# (profiles/), valid only while the kernel source hashes to the recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": None, "traffic_per_algorithmic_byte": None}
+# dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
+# captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
+# batch-64 global layer); used only while the kernel sources hash to the recorded value
+NCU_DECODE_TRAFFIC = {"source_sha1": "5d48207651328345dc4555fb5475495fdc3b56fc",
+                      "per_algorithmic_byte": {"sliding": 1.0242, "global": 1.0384}}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -475,27 +477,34 @@ def run_native(args):
     ms = max_over_ranks(ms, world)
     value = world * work / (ms * 1e-3) / scale
 
-    # roofline of the dominant kernel: the attention launch (row kernel + combine when split)
+    # roofline of the dominant kernel: the attention launch of the layer kind with the largest
+    # share of time (rows_attn_bf16_kernel plus its split combine)
     if decode:
         per_bytes = [decode_bytes(w, l) for l in range(w.n_layers)]
-        achieved = sum(per_bytes) / (sum(launch_ms) * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
-        traffic = None
-        if NCU_DECODE_TRAFFIC["source_sha1"] == kernel_source_sha1():
-            traffic = NCU_DECODE_TRAFFIC["traffic_per_algorithmic_byte"] * sum(per_bytes) / w.n_layers
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "kernel": "attention launch (rows_attn_bf16_kernel + split combine)",
-                "algorithmic_bytes_per_launch": sum(per_bytes) / w.n_layers,
-                "launch_us": 1e3 * sum(launch_ms) / w.n_layers, "peak_source": peak_src}
+        kinds = {}
         for kind, name in ((synth.SLIDING, "sliding"), (synth.GLOBAL, "global")):
             ls = [l for l, s in enumerate(w.layers) if s.kind == kind]
-            if not ls:
-                continue
-            b = sum(per_bytes[l] for l in ls) / len(ls)
-            t = sum(launch_ms[l] for l in ls) / len(ls)
-            roof[name] = {"bytes_per_launch": b, "launch_us": 1e3 * t,
-                          "achieved_gbs": b / (t * 1e-3) / 1e9}
+            if ls:
+                kinds[name] = (sum(per_bytes[l] for l in ls), sum(launch_ms[l] for l in ls), len(ls),
+                               w.layers[ls[0]].head_dim)
+        dom = max(kinds, key=lambda k: kinds[k][1])
+        b, t, n, d = kinds[dom]
+        achieved = b / (t * 1e-3) / 1e9
+        traffic = None
+        if NCU_DECODE_TRAFFIC["source_sha1"] == kernel_source_sha1():
+            traffic = NCU_DECODE_TRAFFIC["per_algorithmic_byte"][dom] * b / n
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": f"rows_attn_bf16_kernel<{d}> + split combine ({dom} layers)",
+                "algorithmic_bytes_per_launch": b / n, "launch_us": 1e3 * t / n,
+                "peak_source": peak_src}
+        for name, (bk, tk, nk, dk) in kinds.items():
+            roof[name] = {"bytes_per_launch": bk / nk, "launch_us": 1e3 * tk / nk,
+                          "achieved_gbs": bk / (tk * 1e-3) / 1e9,
+                          "frac": bk / (tk * 1e-3) / 1e9 / peak}
+        roof["all_layers"] = {"achieved_gbs": sum(per_bytes) / (sum(launch_ms) * 1e-3) / 1e9,
+                              "frac": sum(per_bytes) / (sum(launch_ms) * 1e-3) / 1e9 / peak}
     else:
         per_flops = [prefill_flops(w, l) for l in range(w.n_layers)]
         achieved = sum(per_flops) / (sum(launch_ms) * 1e-3) / 1e12
