@@ -269,12 +269,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The slowest rank's time: the job's step time (no data-path collective; only this)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.item()
+
+
+def job_value(work_per_rank, world, ms_max, scale):
+    """Whole-job throughput: every rank processes its own replica of the workload (weak
+    scaling), so the job moves world x work in the slowest rank's time."""
+    return world * work_per_rank / (ms_max * 1e-3) / scale
 
 
 def build_library(world, local):
@@ -475,7 +483,7 @@ def run_native(args):
     ms, launch_ms, clk, info = timed_graph_run(w, phys, args.steps, args.warmup, device, world,
                                                per_launch=True)
     ms = max_over_ranks(ms, world)
-    value = world * work / (ms * 1e-3) / scale
+    value = job_value(work, world, ms, scale)
 
     # roofline of the dominant kernel: the attention launch of the layer kind with the largest
     # share of time (rows_attn_bf16_kernel plus its split combine)
