@@ -181,7 +181,7 @@ class DeviceState:
         msl = max(w.ctx_lens)
         ws = max(g.gemma_attn_workspace_size(B, s.kind, s.window, s.n_q, s.n_kv, s.head_dim, msl,
                                              w.n_new) for s in w.layers)
-        self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
         self.max_seq_len = msl
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.cache_bytes = sum(t.numel() * t.element_size() for t in

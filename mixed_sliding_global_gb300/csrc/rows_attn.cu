@@ -457,41 +457,84 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
 // split-K combine (decode): merge the per-chunk (m, l, O) of each (sequence, query head)
 //   M = max_c m_c,  w_c = 2^(m_c - M),  out = sum_c w_c O_c / sum_c w_c l_c
 // ---------------------------------------------------------------------------------------------
+// One CTA per (query head, sequence). The chunk weights w_c and their sum are computed once
+// into shared memory; then 4 groups of threads each accumulate a quarter of the chunks for
+// every column (loads unrolled, so a group keeps several L2 reads in flight), and the groups
+// are summed through shared memory.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineGroups = 4;
+
 template <typename OutT>
-__global__ void combine_kernel(const RowsParams p, int D) {
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const RowsParams p, int D) {
+    __shared__ float s_w[128];                                  // chunk weights (n_split <= 128)
+    __shared__ float s_red[kCombineGroups][kCombineThreads / kCombineGroups * 4];
+    __shared__ float s_inv;
     const int head = blockIdx.x, b = blockIdx.y;
     const int len = __ldg(p.seq_lens + b);
     OutT* dst = reinterpret_cast<OutT*>(p.out) + ((size_t)b * p.n_q + head) * (size_t)D;
-    const int col = threadIdx.x * 4;
+    const int tid = threadIdx.x;
     if (len < 1 || len > p.cap || len > p.max_seq_len) {
-        if (col < D)
-            for (int e = 0; e < 4; ++e) dst[col + e] = OutT(0.f);
+        for (int c = tid; c < D; c += blockDim.x) dst[c] = OutT(0.f);
         return;
     }
     const int lo = p.is_sliding ? max(0, len - p.window) : 0;
     const int nc = min(p.n_split, (len - lo + p.chunk - 1) / p.chunk);
     const size_t base = ((size_t)b * p.n_q + head) * p.n_split;
-    float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, p.ml_part[(base + c) * 2]);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < nc; ++c) {
-        const float w = exp2f(p.ml_part[(base + c) * 2] - M);
-        L = fmaf(w, p.ml_part[(base + c) * 2 + 1], L);
-        if (col < D) {
+    if (tid < 32) {
+        // warp 0: M = max_c m_c, w_c = 2^(m_c - M), L = sum_c w_c l_c
+        float m[4], l[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = tid + 32 * i;
+            m[i] = c < nc ? p.ml_part[(base + c) * 2] : -INFINITY;
+            l[i] = c < nc ? p.ml_part[(base + c) * 2 + 1] : 0.f;
+        }
+        const float M = warp_max(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])));
+        float L = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = tid + 32 * i;
+            const float w = c < nc ? exp2f(m[i] - M) : 0.f;
+            if (c < 128) s_w[c] = w;
+            L = fmaf(w, l[i], L);
+        }
+        L = warp_sum(L);
+        if (tid == 0) s_inv = 1.f / L;
+    }
+    __syncthreads();
+    const int per_group = kCombineThreads / kCombineGroups;  // threads per chunk group
+    const int grp = tid / per_group, col4 = tid - grp * per_group;
+    for (int cb = 0; cb < D; cb += per_group * 4) {  // same trip count for every thread
+        const int col = cb + col4 * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int c = grp; c < nc && col < D; c += kCombineGroups) {
+            const float w = s_w[c];
             const float4 v = *reinterpret_cast<const float4*>(p.o_part + (base + c) * D + col);
             acc.x = fmaf(w, v.x, acc.x);
             acc.y = fmaf(w, v.y, acc.y);
             acc.z = fmaf(w, v.z, acc.z);
             acc.w = fmaf(w, v.w, acc.w);
         }
-    }
-    if (col < D) {
-        const float inv = 1.f / L;
-        dst[col + 0] = OutT(acc.x * inv);
-        dst[col + 1] = OutT(acc.y * inv);
-        dst[col + 2] = OutT(acc.z * inv);
-        dst[col + 3] = OutT(acc.w * inv);
+        *reinterpret_cast<float4*>(&s_red[grp][col4 * 4]) = acc;
+        __syncthreads();
+        if (grp == 0 && col < D) {
+            float4 t = *reinterpret_cast<const float4*>(&s_red[0][col4 * 4]);
+#pragma unroll
+            for (int g2 = 1; g2 < kCombineGroups; ++g2) {
+                const float4 u = *reinterpret_cast<const float4*>(&s_red[g2][col4 * 4]);
+                t.x += u.x;
+                t.y += u.y;
+                t.z += u.z;
+                t.w += u.w;
+            }
+            const float inv = s_inv;
+            dst[col + 0] = OutT(t.x * inv);
+            dst[col + 1] = OutT(t.y * inv);
+            dst[col + 2] = OutT(t.z * inv);
+            dst[col + 3] = OutT(t.w * inv);
+        }
+        __syncthreads();
     }
 }
 
@@ -565,7 +608,7 @@ cudaError_t launch_rows_f32(const RowsParams& p, int head_dim, dim3 grid, cudaSt
 cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out_fp32,
                            cudaStream_t st) {
     const dim3 grid(p.n_q, batch);
-    const dim3 block(head_dim / 4 < 32 ? 32 : head_dim / 4);
+    const dim3 block(kCombineThreads);
     if (out_fp32)
         combine_kernel<float><<<grid, block, 0, st>>>(p, head_dim);
     else

@@ -95,7 +95,7 @@ class GpuRun:
         B = q.shape[0]
         ws_n = self.g.gemma_attn_workspace_size(B, spec.kind, spec.window, spec.n_q, spec.n_kv,
                                                 spec.head_dim, msl, w.n_new)
-        ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=q.device)
+        ws = torch.zeros(max(ws_n, 1), dtype=torch.uint8, device=q.device)
         fn = self.g.gemma_attn_decode if w.n_new == 1 else self.g.gemma_attn_prefill
         fn(out, q, self.kc, self.vc, w.owner_map, l, d["seq_lens"], msl, kind=spec.kind,
            window=spec.window, n_kv=spec.n_kv, k_eq_v=spec.k_eq_v, scale=w.scale(l),

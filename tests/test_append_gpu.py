@@ -69,7 +69,7 @@ def test_seq_len_beyond_hint_is_reported_and_zeroed():
     lens = torch.tensor([100, 200], dtype=torch.int32, device="cuda")
     out = torch.full_like(q, 7.0)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     g.gemma_attn_decode(out, q, [kc], None, [0], 0, lens, 150, kind=g.GEMMA_GLOBAL, window=0,
                         n_kv=1, k_eq_v=True, scale=0.1, workspace=ws, device_error=err)
     torch.cuda.synchronize()

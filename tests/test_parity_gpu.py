@@ -174,3 +174,29 @@ def test_split_plan_does_not_change_the_result(spec):
         torch.cuda.synchronize()
         compare(outs[-1], ref, BF16)
     assert (outs[0].float() - outs[1].float()).abs().max().item() <= 2e-2
+
+
+def test_workspace_is_reusable_across_calls():
+    """The workspace holds no state between calls: consecutive decode calls with different batch
+    and split plans on one workspace match calls on fresh workspaces bit for bit."""
+    import mixed_sliding_global_gb300 as g
+    cases = [(LayerSpec(GLOBAL, 0, 16, 1, 512, True), [3000, 5000, 777], 5056),
+             (LayerSpec(SLIDING, 1024, 16, 8, 256, False), [4000, 1500], 4032),
+             (LayerSpec(GLOBAL, 0, 16, 1, 512, True), [9000], 9024)]
+    shared = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for spec, lens, cap in cases:
+            w = one_layer(spec, 1, lens, cap)
+            hb = host_inputs(w, [0])
+            gr = GpuRun(w, hb)
+            gr.append(0)
+            fresh = gr.attend(0)
+            d = gr.dev[0]
+            out = torch.empty_like(fresh)
+            g.gemma_attn_decode(out, d["q"], gr.kc, gr.vc, [0], 0, d["seq_lens"], max(lens),
+                                kind=spec.kind, window=spec.window, n_kv=spec.n_kv,
+                                k_eq_v=spec.k_eq_v, scale=w.scale(0), workspace=shared,
+                                device_error=gr.err)
+            torch.cuda.synchronize()
+            assert gr.err.item() == 0
+            assert torch.equal(out, fresh), (rep, spec)

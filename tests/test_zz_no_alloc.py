@@ -51,7 +51,7 @@ def test_static_scratch_decode_matches_workspace_decode(spec, lens, cap):
         ws_n = g.gemma_attn_workspace_size(len(lens), spec.kind, spec.window, spec.n_q,
                                            spec.n_kv, spec.head_dim, msl, 1)
         assert ws_n > 0, "the case must use split scratch"
-        ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(ws_n, dtype=torch.uint8, device="cuda")
         ref = torch.empty_like(q)
         got = torch.full_like(q, float("nan"))
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
