@@ -194,18 +194,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 k_begin + t * kTcKeys, row3, &kv_full[slot]);
             };
             bool ok = true;
+            // ring cursors (slot, phase of the current pass, whether a pass has completed):
+            // kept incrementally, no division by the runtime ring sizes
+            int ks = 0, vs = 0;
+            uint32_t kph = 0, vph = 0;
+            bool kwrap = false, vwrap = false;
             for (int i = 0; i <= n_tiles && ok; ++i) {
                 const int tk = i;          // K tile issued at step i
                 const int tv = i - 1;      // V tile issued at step i
                 if (tk < n_tiles) {
-                    const int sl = tk % NK;
-                    if (tk >= NK) ok = mbar_wait(&kv_empty[sl], ((tk / NK) - 1) & 1, p.err);
-                    if (ok) load(&kmap, sl, tk);
+                    if (kwrap) ok = mbar_wait(&kv_empty[ks], kph ^ 1u, p.err);
+                    if (ok) load(&kmap, ks, tk);
+                    if (++ks == NK) {
+                        ks = 0;
+                        kph ^= 1u;
+                        kwrap = true;
+                    }
                 }
                 if (!p.k_eq_v && tv >= 0 && ok) {
-                    const int sl = NK + tv % NV;
-                    if (tv >= NV) ok = mbar_wait(&kv_empty[sl], ((tv / NV) - 1) & 1, p.err);
-                    if (ok) load(&vmap, sl, tv);
+                    if (vwrap) ok = mbar_wait(&kv_empty[NK + vs], vph ^ 1u, p.err);
+                    if (ok) load(&vmap, NK + vs, tv);
+                    if (++vs == NV) {
+                        vs = 0;
+                        vph ^= 1u;
+                        vwrap = true;
+                    }
                 }
             }
         }
@@ -227,11 +240,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
         };
+        // ring cursors of the consumer side: K slot and phase for S = Q K^T, V slot and phase
+        // for P V, and (with K as V) the slot of the previous K tile
+        int mk = 0, mv = 0, k_prev = 0;
+        uint32_t mkph = 0, mvph = 0;
         auto issue_pv = [&](int j) {
             if (ok) ok = mbar_wait(p_full, j & 1, p.err);
-            const int sv = p.k_eq_v ? j % NK : NK + j % NV;
+            const int sv = p.k_eq_v ? k_prev : NK + mv;
+            const uint32_t sv_phase = mvph;
+            if (!p.k_eq_v && ++mv == NV) {
+                mv = 0;
+                mvph ^= 1u;
+            }
             if (ok && !p.k_eq_v) {
-                ok = mbar_wait(&kv_full[sv], (j / NV) & 1, p.err);
+                ok = mbar_wait(&kv_full[sv], sv_phase, p.err);
                 const int n_valid = k_end - (k_begin + j * kTcKeys);
                 if (n_valid < kTcKeys) zero_tail(slots + sv * Lay::SLOT, n_valid);
             }
@@ -252,8 +274,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
         };
         for (int t = 0; t < n_tiles; ++t) {
-            const int sk = t % NK;
-            if (ok) ok = mbar_wait(&kv_full[sk], (t / NK) & 1, p.err);
+            const int sk = mk;
+            if (ok) ok = mbar_wait(&kv_full[sk], mkph, p.err);
+            if (++mk == NK) {
+                mk = 0;
+                mkph ^= 1u;
+            }
             if (p.k_eq_v) {
                 const int n_valid = k_end - (k_begin + t * kTcKeys);
                 if (n_valid < kTcKeys) zero_tail(slots + sk * Lay::SLOT, n_valid);
@@ -274,6 +300,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             __syncwarp();
             if (t >= 1) issue_pv(t - 1);
+            k_prev = sk;
         }
         if (n_tiles > 0) issue_pv(n_tiles - 1);
     } else {
