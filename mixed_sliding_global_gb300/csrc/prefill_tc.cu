@@ -22,14 +22,20 @@
 // CL = 2 (head_dim 512): a 128 x 512 fp32 O alone would fill the 512 TMEM columns of an SM,
 // so a cluster of two CTAs splits head_dim: CTA h holds Q[:, 256h:256h+256] and reads only
 // that half of K and V. Each computes a partial S over its half, sends it to its peer through
-// distributed shared memory (fp32), and adds the peer's partial to its own: both CTAs obtain
-// bit-identical S (IEEE addition commutes), hence identical P, m and l, and each accumulates
-// and writes its own half of O. No multiply-add is done twice. With k_eq_v the K half is also
-// the V half.
+// distributed shared memory, and adds the peer's partial to its own; each then accumulates and
+// writes its own half of O with its own P, m and l. No multiply-add is done twice. With k_eq_v
+// the K half is also the V half.
+// The partial scores travel as fp16 (saturating): the exchange, not the tensor core, bounds
+// these clusters, and fp16 halves its bytes. Each CTA keeps its own partial in fp32; the peer's
+// rounding moves a score by at most 2^-11 of its partial (for |partial| <= 128 raw, <= 0.06 raw,
+// i.e. < 0.4% in exp(scale * s) at scale 1/sqrt(512)), the size of the bf16 rounding P already
+// gets before P V.
 //
 // The key range of the tile is clamped to [first row's window start, last row's position]
 // before any load; rows of the last partial key tile beyond the range are zeroed in shared
 // memory before they enter P V.
+#include <cuda_fp16.h>
+
 #include "attn_internal.h"
 #include "tc.cuh"
 #include "tmap.h"
@@ -53,7 +59,7 @@ struct TcLayout {
     static constexpr int CHUNKS = DH / 64;               // 64-column boxes per K/V tile
     static constexpr int SLOT = CHUNKS * kTcKeys * 128;  // bytes of one K or V tile
     static constexpr int P_BYTES = kTcKeys * 128 * 2;    // 128 rows x 128 keys bf16
-    static constexpr int X_BYTES = CL > 1 ? 128 * kTcKeys * 4 : 0;  // peer's partial S (fp32)
+    static constexpr int X_BYTES = CL > 1 ? 128 * kTcKeys * 2 : 0;  // peer's partial S (fp16)
     static constexpr int Q_COL = 0;                      // TMEM columns
     static constexpr int S_COL = 128;
     static constexpr int O_COL = 256;
@@ -76,10 +82,21 @@ GEMMA_DEVINL uint32_t map_to_peer(const void* local, uint32_t peer) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(peer));
     return r;
 }
-GEMMA_DEVINL void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
+GEMMA_DEVINL void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
                  : "memory");
+}
+// two fp32 -> packed fp16 (lo in the low half), round to nearest; values beyond the fp16
+// range saturate to +-65504 instead of becoming infinite
+GEMMA_DEVINL uint32_t pack_f16_sat(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+GEMMA_DEVINL float2 unpack_f16(uint32_t v) {
+    __half2 h = *reinterpret_cast<__half2*>(&v);
+    return __half22float2(h);
 }
 GEMMA_DEVINL void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
@@ -368,22 +385,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (CL > 1) {
                 // send this row's partial scores to the peer, then add the peer's partial
                 if (t >= 1 && ok) ok = mbar_wait_cluster(x_free, (t - 1) & 1, p.err);
-                // chunk-major layout X[c][r] (16-byte chunks): a warp's 32 stores of chunk c
-                // are one contiguous 512-byte write, and the local loads are contiguous too
+                // chunk-major layout X[c][r] (16-byte chunks of 8 fp16 scores): a warp's 32
+                // stores of chunk c are one contiguous 512-byte write, and the local loads are
+                // contiguous too
 #pragma unroll
-                for (int c = 0; c < kTcKeys / 4; ++c)
-                    st_cluster_v4(peer_x + c * (128 * 16), s[4 * c], s[4 * c + 1], s[4 * c + 2],
-                                  s[4 * c + 3]);
+                for (int c = 0; c < kTcKeys / 8; ++c)
+                    st_cluster_v4(peer_x + c * (128 * 16), pack_f16_sat(s[8 * c], s[8 * c + 1]),
+                                  pack_f16_sat(s[8 * c + 2], s[8 * c + 3]),
+                                  pack_f16_sat(s[8 * c + 4], s[8 * c + 5]),
+                                  pack_f16_sat(s[8 * c + 6], s[8 * c + 7]));
                 mbar_arrive_remote(peer_x_full);
                 if (ok) ok = mbar_wait_cluster(x_full, t & 1, p.err);
-                const float4* xr = reinterpret_cast<const float4*>(sX) + r;
+                const uint4* xr = reinterpret_cast<const uint4*>(sX) + r;
 #pragma unroll
-                for (int e = 0; e < kTcKeys / 4; ++e) {
-                    const float4 x = xr[e * 128];
-                    s[4 * e + 0] += x.x;
-                    s[4 * e + 1] += x.y;
-                    s[4 * e + 2] += x.z;
-                    s[4 * e + 3] += x.w;
+                for (int e = 0; e < kTcKeys / 8; ++e) {
+                    const uint4 x = xr[e * 128];
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = unpack_f16(w[i]);
+                        s[8 * e + 2 * i] += f.x;
+                        s[8 * e + 2 * i + 1] += f.y;
+                    }
                 }
                 mbar_arrive_remote(peer_x_free);
             }
