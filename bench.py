@@ -42,8 +42,8 @@ RAGGED_PHYS_LAYERS = 6   # distinct caches for 48 ragged layer-steps (one 5:1 pe
 # dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
 # captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
 # batch-64 global layer); used only while the kernel sources hash to the recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": "5d48207651328345dc4555fb5475495fdc3b56fc",
-                      "per_algorithmic_byte": {"sliding": 1.0242, "global": 1.0384}}
+NCU_DECODE_TRAFFIC = {"source_sha1": "723a40dafacef7b435e19615c10073e117064628",
+                      "per_algorithmic_byte": {"sliding": 1.0197, "global": 1.0376}}
 
 
 # ---------------------------------------------------------------------------------------------
