@@ -15,6 +15,7 @@ def lib():
 
 
 def test_library_exports_every_declared_symbol():
+    lib()  # builds the library first when it is missing or older than its sources
     names = g.exported_symbols()
     assert {"gemma_kv_append", "gemma_attn_decode", "gemma_attn_prefill",
             "gemma_attn_workspace_size", "gemma_status_string", "gemma_abi_version"} <= set(names)
