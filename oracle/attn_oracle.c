@@ -32,14 +32,22 @@
  *  - the new tokens are written into the cache before attention, so the cache
  *    holds len tokens and the i-th of n_tok queries sits at p = len - n_tok + i;
  *  - the softmax scale is an explicit argument (1/sqrt(head_dim) in the
- *    workloads); no logit soft-cap is applied.
+ *    workloads);
+ *  - the attention-logit soft-cap ("Gemma-4 12B on AWS Inferentia2 - Tensor-
+ *    Parallel (TP=2), device prefill": the port keeps an explicit attention
+ *    softcap; no value is given) is optional: with softcap c > 0 each scaled
+ *    score s = scale * q.k becomes c * tanh(s / c) before the softmax; c = 0
+ *    applies none.
  *
  * Parity pins (tests): torch fp64 scaled_dot_product_attention on tiny shapes,
  * closed forms (uniform weights for K = 0, one-hot V, W = 1, two keys), and
  * invariants (W >= len equals global, K-as-V equals passing K as V, shared
  * layer equals a private copy of its owner's cache, one KV head broadcast
- * equals replicated heads, key permutation, key shift). The scale convention
- * of the real model is not pinned by the pages ("parity unpinned" for it).
+ * equals replicated heads, key permutation, key shift); the soft-cap by a cap
+ * far above every score (no change) and by the saturated closed form (scores
+ * of +-L with L >> c become exactly +-c). The scale convention of the real
+ * model, and its soft-cap value, are not pinned by the pages ("parity
+ * unpinned" for them).
  *
  * ORACLE_MUTANT, when defined, plants one deliberate mistake; the test suite
  * builds such variants to show that its pins catch each of them. The normal
@@ -134,11 +142,13 @@ int oracle_kv_append(void* cache, const void* rows, const int32_t* write_pos, in
  *   seq_lens [batch] valid cache tokens after the new tokens were written
  *   out      [batch][n_tok][n_q][head_dim]            (double)
  */
-int oracle_attention(const oracle_layer* layers, const int32_t* owner_map, int n_layers, int layer,
-                     const void* const* k_cache, const void* const* v_cache, int dtype,
-                     int capacity, const void* q, int n_tok, const int32_t* seq_lens, int batch,
-                     double scale, double* out)
+int oracle_attention_softcap(const oracle_layer* layers, const int32_t* owner_map, int n_layers,
+                             int layer, const void* const* k_cache, const void* const* v_cache,
+                             int dtype, int capacity, const void* q, int n_tok,
+                             const int32_t* seq_lens, int batch, double scale, double softcap,
+                             double* out)
 {
+    if (!(softcap >= 0.0) || isinf(softcap)) return ORACLE_ERR_ARG;
     /* 1. which layer's cache this layer reads */
     int o = oracle_resolve_owner(layers, owner_map, n_layers, layer);
     if (o < 0) return o;
@@ -229,6 +239,13 @@ int oracle_attention(const oracle_layer* layers, const int32_t* owner_map, int n
 #if ORACLE_MUTANT == 2
                     s[j] = dot; /* planted mistake: scale dropped */
 #endif
+                    /* 5a. optional soft-cap of the scaled score */
+                    if (softcap > 0.0) {
+                        s[j] = softcap * tanh(s[j] / softcap);
+#if ORACLE_MUTANT == 8
+                        s[j] = scale * softcap * tanh(dot / softcap); /* planted: cap before scale */
+#endif
+                    }
                     if (s[j] > m) m = s[j];
                 }
                 double denom = 0.0;
@@ -258,4 +275,14 @@ int oracle_attention(const oracle_layer* layers, const int32_t* owner_map, int n
     }
     free(kv_of);
     return status;
+}
+
+/* oracle_attention_softcap without a soft-cap. */
+int oracle_attention(const oracle_layer* layers, const int32_t* owner_map, int n_layers, int layer,
+                     const void* const* k_cache, const void* const* v_cache, int dtype,
+                     int capacity, const void* q, int n_tok, const int32_t* seq_lens, int batch,
+                     double scale, double* out)
+{
+    return oracle_attention_softcap(layers, owner_map, n_layers, layer, k_cache, v_cache, dtype,
+                                    capacity, q, n_tok, seq_lens, batch, scale, 0.0, out);
 }

@@ -76,6 +76,9 @@ class Oracle:
             ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
             ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
             ctypes.c_int, ctypes.c_double, ctypes.c_void_p]
+        lib.oracle_attention_softcap.restype = ctypes.c_int
+        lib.oracle_attention_softcap.argtypes = lib.oracle_attention.argtypes[:-1] + [
+            ctypes.c_double, ctypes.c_void_p]
         lib.oracle_kv_append.restype = ctypes.c_int
         lib.oracle_kv_append.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_int,
@@ -108,8 +111,10 @@ class Oracle:
     def attention(self, layers, owner_map: Sequence[int], layer: int,
                   k_caches: Sequence[Optional[torch.Tensor]],
                   v_caches: Sequence[Optional[torch.Tensor]],
-                  q: torch.Tensor, seq_lens: Sequence[int], scale: float) -> torch.Tensor:
+                  q: torch.Tensor, seq_lens: Sequence[int], scale: float,
+                  softcap: float = 0.0) -> torch.Tensor:
         """q [B][n_tok][n_q][d]; k_caches[o] [B][n_kv][cap][d] for owner layers (None elsewhere).
+        softcap > 0 caps each scaled score s to softcap * tanh(s / softcap); 0 applies none.
         Returns fp64 [B][n_tok][n_q][d]."""
         n_layers = len(layers)
         B, n_tok, n_q, d = q.shape
@@ -128,8 +133,9 @@ class Oracle:
         om = (ctypes.c_int32 * n_layers)(*[int(x) for x in owner_map])
         arr = (_Layer * n_layers)(*oracle_layers(layers))
         out = torch.empty((B, n_tok, n_q, d), dtype=torch.float64)
-        st = self.lib.oracle_attention(arr, om, n_layers, layer, kp, vp, dt, cap, _ptr(q), n_tok,
-                                       sl, B, float(scale), _ptr(out))
+        st = self.lib.oracle_attention_softcap(arr, om, n_layers, layer, kp, vp, dt, cap, _ptr(q),
+                                               n_tok, sl, B, float(scale), float(softcap),
+                                               _ptr(out))
         if st != 0:
             raise OracleError(f"oracle_attention status {st}")
         return out

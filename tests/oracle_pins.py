@@ -215,6 +215,47 @@ def pin_two_keys(orc):
 
 
 # ---------------------------------------------------------------------------------------------
+# the optional attention-logit soft-cap: c * tanh(s / c) of the scaled score s
+# ---------------------------------------------------------------------------------------------
+def pin_softcap_far_above_scores_changes_nothing(orc):
+    """A cap far above every score leaves the result unchanged: c tanh(s / c) differs from s
+    by about s^3 / (3 c^2), here below 1e-10 for |s| < 10."""
+    d = 32
+    spec = L(SLIDING, 5, 4, 2, d)
+    q = _rand((2, 3, 4, d), 71)
+    kc = _cache(2, 2, 12, d, 72)
+    vc = _cache(2, 2, 12, d, 73)
+    lens, scale = [12, 9], 1.0 / math.sqrt(d)
+    plain = orc.attention([spec], [0], 0, [kc], [vc], q, lens, scale)
+    capped = orc.attention([spec], [0], 0, [kc], [vc], q, lens, scale, softcap=1.0e6)
+    assert (plain - capped).abs().max().item() < 1e-9
+
+
+def pin_softcap_saturated_scores(orc):
+    """Scaled scores of +-L with L far above the cap become exactly +-c (tanh of +-5000 is +-1
+    in double precision), so with one-hot value rows the output is the weight vector
+    e^(+-c) / (n_plus e^c + n_minus e^-c). The scale is applied before the cap: scale 0.5 and
+    q . k = +-2e4 give s = +-1e4."""
+    d, c, scale = 8, 2.0, 0.5
+    signs = [1, -1, 1, 1, -1, 1]
+    n = len(signs)
+    spec = L(GLOBAL, 0, 1, 1, d)
+    q = torch.zeros(1, 1, 1, d)
+    q[0, 0, 0, 0] = 1.0
+    kc = torch.zeros(1, 1, n, d)
+    vc = torch.zeros(1, 1, n, d)
+    for j, sg in enumerate(signs):
+        kc[0, 0, j, 0] = 2.0e4 * sg
+        vc[0, 0, j, j] = 1.0
+    got = orc.attention([spec], [0], 0, [kc], [vc], q, [n], scale, softcap=c)
+    n_plus, n_minus = signs.count(1), signs.count(-1)
+    den = n_plus * math.exp(c) + n_minus * math.exp(-c)
+    for j, sg in enumerate(signs):
+        assert abs(got[0, 0, 0, j].item() - math.exp(c * sg) / den) < 1e-15, j
+    assert got[0, 0, 0, n:].abs().max().item() == 0.0
+
+
+# ---------------------------------------------------------------------------------------------
 # invariants
 # ---------------------------------------------------------------------------------------------
 def pin_window_covering_context_is_global(orc):
