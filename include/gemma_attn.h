@@ -160,6 +160,26 @@ int gemma_attn_prefill(void* out, const void* q, const void* const* k_cache,
                        uint32_t* device_error, void* stream);
 
 /*
+ * gemma_attn_softcap -- gemma_attn_decode (n_new == 1) or gemma_attn_prefill (n_new > 1) with
+ * an attention-logit soft-cap: each scaled score s = scale * q . k becomes
+ * softcap * tanh(s / softcap) before the softmax. Source: "Gemma-4 12B on AWS Inferentia2 -
+ * Tensor-Parallel (TP=2), device prefill" (the port keeps an explicit attention softcap; the
+ * page gives no value, so it is the caller's argument).
+ *   softcap           finite and >= 0; 0 applies no cap (the call then equals the entry point
+ *                     without a cap). Negative or non-finite values return
+ *                     GEMMA_ERR_INVALID_ARG.
+ *   Other arguments, the workspace size and the results are those of gemma_attn_decode /
+ *   gemma_attn_prefill for the same n_new.
+ */
+int gemma_attn_softcap(void* out, const void* q, const void* const* k_cache,
+                       const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                       int layer, const int32_t* seq_lens, int max_seq_len, int n_new,
+                       int batch, gemma_layer_kind kind, int window, int n_q, int n_kv,
+                       int head_dim, int k_eq_v, int kv_capacity, float scale, float softcap,
+                       gemma_dtype dtype, void* workspace, size_t workspace_bytes,
+                       uint32_t* device_error, void* stream);
+
+/*
  * gemma_attn_workspace_size -- bytes of scratch that gemma_attn_decode (n_new == 1) or
  * gemma_attn_prefill (n_new > 1) needs for these arguments on the current device (the split
  * plan depends on its SM count). Returns 0 when no scratch is needed and (size_t)-1 when the

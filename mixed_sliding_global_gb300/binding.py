@@ -35,6 +35,10 @@ _SIGNATURES = {
                                           _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_int,
                                           _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                                           _c_void_p, _c_void_p]),
+    "gemma_attn_softcap": (_c_int, [_c_void_p, _c_void_p, _PVOID, _PVOID, _PI32, _c_int, _c_int,
+                                    _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                    _c_int, _c_int, _c_int, _c_int, _c_float, _c_float, _c_int,
+                                    _c_void_p, _c_size_t, _c_void_p, _c_void_p]),
     "gemma_attn_workspace_size": (_c_size_t, [_c_int] * 8),
     "gemma_status_string": (ctypes.c_char_p, [_c_int]),
     "gemma_abi_version": (_c_int, []),
@@ -157,7 +161,8 @@ def gemma_attn_workspace_size(batch: int, kind: int, window: int, n_q: int, n_kv
 
 
 def _attn(fn_name, out, q, k_cache, v_cache, owner_map, layer, seq_lens, max_seq_len, n_tok, *,
-          kind, window, n_kv, k_eq_v, scale, kv_capacity, workspace, device_error, stream):
+          kind, window, n_kv, k_eq_v, scale, kv_capacity, workspace, device_error, stream,
+          softcap=None):
     B = q.shape[0]
     n_q, d = q.shape[-2], q.shape[-1]
     n_layers = len(owner_map)
@@ -173,6 +178,9 @@ def _attn(fn_name, out, q, k_cache, v_cache, owner_map, layer, seq_lens, max_seq
             _dtype(q), ws_ptr, ws_bytes, _dev_ptr(device_error), _stream(stream))
     if fn_name == "gemma_attn_decode":
         st = lib.gemma_attn_decode(_dev_ptr(out), _dev_ptr(q), *common, *tail)
+    elif fn_name == "gemma_attn_softcap":
+        st = lib.gemma_attn_softcap(_dev_ptr(out), _dev_ptr(q), *common, int(n_tok), *tail[:9],
+                                    float(softcap), *tail[9:])
     else:
         st = lib.gemma_attn_prefill(_dev_ptr(out), _dev_ptr(q), *common, int(n_tok), *tail)
     _check(fn_name, st)
@@ -198,6 +206,19 @@ def gemma_attn_prefill(out: torch.Tensor, q: torch.Tensor, k_cache, v_cache, own
     _attn("gemma_attn_prefill", out, q, k_cache, v_cache, owner_map, layer, seq_lens, max_seq_len,
           q.shape[1], kind=kind, window=window, n_kv=n_kv, k_eq_v=k_eq_v, scale=scale,
           kv_capacity=kv_capacity, workspace=workspace, device_error=device_error, stream=stream)
+
+
+def gemma_attn_softcap(out: torch.Tensor, q: torch.Tensor, k_cache, v_cache, owner_map,
+                       layer: int, seq_lens: torch.Tensor, max_seq_len: int, *, kind: int,
+                       window: int, n_kv: int, k_eq_v: bool, scale: float, softcap: float,
+                       kv_capacity: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
+                       device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Decode (q.shape[1] == 1) or prefill with each scaled score s capped to
+    softcap * tanh(s / softcap) (softcap 0: no cap). q, out: [B][n_tok][n_q][d]."""
+    _attn("gemma_attn_softcap", out, q, k_cache, v_cache, owner_map, layer, seq_lens, max_seq_len,
+          q.shape[1], kind=kind, window=window, n_kv=n_kv, k_eq_v=k_eq_v, scale=scale,
+          kv_capacity=kv_capacity, workspace=workspace, device_error=device_error, stream=stream,
+          softcap=softcap)
 
 
 def gemma_attn_decode_static(out: torch.Tensor, q: torch.Tensor, k_cache, v_cache, owner_map,

@@ -98,9 +98,10 @@ Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim,
 int attention(void* out, const void* q, const void* const* k_cache, const void* const* v_cache,
               const int32_t* owner_map, int n_layers, int layer, const int32_t* seq_lens,
               int max_seq_len, int n_tok, int batch, int kind, int window, int n_q, int n_kv,
-              int head_dim, int k_eq_v, int kv_capacity, float scale, int dtype, void* workspace,
-              size_t workspace_bytes, uint32_t* device_error, void* stream) {
+              int head_dim, int k_eq_v, int kv_capacity, float scale, float softcap, int dtype,
+              void* workspace, size_t workspace_bytes, uint32_t* device_error, void* stream) {
     if (batch < 0 || n_tok < 1) return GEMMA_ERR_INVALID_ARG;
+    if (!std::isfinite(softcap) || softcap < 0.f) return GEMMA_ERR_INVALID_ARG;
     int st = check_shape(kind, window, n_q, n_kv, head_dim, dtype);
     if (st != GEMMA_OK) return st;
     int o = 0;
@@ -151,6 +152,9 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     p.chunk = pl.chunk;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.softcap = softcap;
+    p.cap_inner = softcap > 0.f ? scale / softcap : 0.f;
+    p.cap_log2 = softcap * 1.4426950408889634f;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const long long rows = (long long)n_tok * p.G;
     cudaError_t e;
@@ -229,7 +233,7 @@ int gemma_attn_decode(void* out, const void* q, const void* const* k_cache,
                       void* workspace, size_t workspace_bytes, uint32_t* device_error,
                       void* stream) {
     return attention(out, q, k_cache, v_cache, owner_map, n_layers, layer, seq_lens, max_seq_len,
-                     1, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
+                     1, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale, 0.f,
                      dtype, workspace, workspace_bytes, device_error, stream);
 }
 
@@ -243,7 +247,20 @@ int gemma_attn_prefill(void* out, const void* q, const void* const* k_cache,
     if (n_new == 0 && batch >= 0) return GEMMA_OK;
     return attention(out, q, k_cache, v_cache, owner_map, n_layers, layer, seq_lens, max_seq_len,
                      n_new, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
-                     dtype, workspace, workspace_bytes, device_error, stream);
+                     0.f, dtype, workspace, workspace_bytes, device_error, stream);
+}
+
+int gemma_attn_softcap(void* out, const void* q, const void* const* k_cache,
+                       const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                       int layer, const int32_t* seq_lens, int max_seq_len, int n_new,
+                       int batch, gemma_layer_kind kind, int window, int n_q, int n_kv,
+                       int head_dim, int k_eq_v, int kv_capacity, float scale, float softcap,
+                       gemma_dtype dtype, void* workspace, size_t workspace_bytes,
+                       uint32_t* device_error, void* stream) {
+    if (n_new == 0 && batch >= 0) return GEMMA_OK;
+    return attention(out, q, k_cache, v_cache, owner_map, n_layers, layer, seq_lens, max_seq_len,
+                     n_new, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
+                     softcap, dtype, workspace, workspace_bytes, device_error, stream);
 }
 
 size_t gemma_attn_workspace_size(int batch, gemma_layer_kind kind, int window, int n_q,

@@ -27,6 +27,12 @@ struct RowsParams {
     int n_stages;             // smem pipeline depth (bf16 kernel)
     float scale_log2;         // softmax scale * log2(e)
     float scale;              // softmax scale
+    // optional attention-logit soft-cap c (0: none): a scaled score s becomes c * tanh(s / c);
+    // kernels evaluate it on the raw dot product r as cap_log2 * tanh(r * cap_inner), already
+    // in log2 units (cap_inner = scale / c, cap_log2 = c * log2(e))
+    float softcap;
+    float cap_inner;
+    float cap_log2;
 };
 
 // Keys per shared-memory tile of the bf16 kernel; chunks are multiples of it.

@@ -126,7 +126,9 @@ GEMMA_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* er
     }
 }
 
-template <int D, int CL>
+// SOFTCAP: the soft-capped variant (a separate instantiation, so that the plain kernel carries
+// no code for it)
+template <int D, int CL, bool SOFTCAP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const TcParams tp) {
@@ -411,7 +413,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_arrive_remote(peer_x_free);
             }
 
-            // scores stay raw; scale > 0, so max(raw) * scale_log2 is the max of scaled scores
+            // scores stay raw; scale > 0, so max(raw) * scale_log2 is the max of scaled scores.
+            // With a soft-cap they are first mapped to c * tanh(scale * raw / c) in log2 units
+            // (before the mask, so masked keys stay -inf).
+            float sl2 = p.scale_log2;
+            if (SOFTCAP) {
+#pragma unroll
+                for (int e = 0; e < kTcKeys; ++e) s[e] = p.cap_log2 * tanhf(s[e] * p.cap_inner);
+                sl2 = 1.f;
+            }
             const int kt0 = k_begin + t * kTcKeys;
             const bool full = kt0 >= lo && kt0 + kTcKeys <= hi;
             if (!full) {
@@ -430,7 +440,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[e + i]);
             const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                             p.scale_log2;
+                             sl2;
             const bool need = mx > m_ref + kLazyRescaleLog2;
             const float m_new = need ? mx : m_ref;
             if (t > 0 && ok) ok = mbar_wait(o_done, (t - 1) & 1, p.err);
@@ -461,8 +471,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int k0 = kb * 64 + c * 8 + 2 * e;
-                        const float p0 = fast_exp2(fmaf(s[k0], p.scale_log2, neg_m));
-                        const float p1 = fast_exp2(fmaf(s[k0 + 1], p.scale_log2, neg_m));
+                        const float p0 = fast_exp2(fmaf(s[k0], sl2, neg_m));
+                        const float p1 = fast_exp2(fmaf(s[k0 + 1], sl2, neg_m));
                         sum4[e] += p0 + p1;
                         w[e] = pack_bf16(p0, p1);
                     }
@@ -541,8 +551,11 @@ static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemLimit);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemLimit);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
@@ -559,7 +572,8 @@ static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL>, km, vm, tp);
+    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, true>, km, vm, tp)
+                           : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, false>, km, vm, tp);
 }
 
 bool prefill_tc_supported(int head_dim) {

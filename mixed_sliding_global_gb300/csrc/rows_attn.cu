@@ -279,7 +279,10 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
 #pragma unroll
                 for (int kq = 0; kq < KSPLIT; ++kq)
                     sv += sS[(kq * kRowTile + r) * Lay::S_STRIDE + lane];
-                sv = valid ? sv * p.scale_log2 : -INFINITY;
+                // scaled score in log2 units (soft-capped when a cap is set); masked keys -inf
+                if (!valid) sv = -INFINITY;
+                else if (p.softcap > 0.f) sv = p.cap_log2 * tanhf(sv * p.cap_inner);
+                else sv *= p.scale_log2;
                 const float m_new = fmaxf(m_run[rr], warp_max(sv));
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;
                 const float alpha = exp2f(m_run[rr] - m_use);
@@ -429,7 +432,8 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) dot = fmaf(qr[e], K[(size_t)j * D + lane + 32 * e], dot);
-        const float s = warp_sum(dot) * p.scale;
+        float s = warp_sum(dot) * p.scale;
+        if (p.softcap > 0.f) s = p.softcap * tanhf(s / p.softcap);
         const float m_new = fmaxf(m, s);
         const float alpha = expf(m - m_new);
         const float w = expf(s - m_new);

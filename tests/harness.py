@@ -31,7 +31,7 @@ def host_inputs(w: synth.Workload, layers: Sequence[int], seqs: Optional[Sequenc
 
 
 def oracle_outputs(w: synth.Workload, hb: Dict[int, synth.LayerBatch], layers: Sequence[int],
-                   q_range=None) -> Dict[int, torch.Tensor]:
+                   q_range=None, softcap: float = 0.0) -> Dict[int, torch.Tensor]:
     """fp64 oracle outputs [B][n_tok][n_q][d] of each layer, after the oracle's own append of
     the new rows into copies of the owner caches. q_range=(i0, i1) restricts the queries to
     tokens [i0, i1) of the step (exactly: earlier keys are all a query may see)."""
@@ -54,7 +54,8 @@ def oracle_outputs(w: synth.Workload, hb: Dict[int, synth.LayerBatch], layers: S
             i0, i1 = q_range
             q = q[:, i0:i1].contiguous()
             lens = [x - w.n_new + i1 for x in lens]
-        out[l] = orc.attention(w.layers, w.owner_map, l, kcs, vcs, q, lens, w.scale(l))
+        out[l] = orc.attention(w.layers, w.owner_map, l, kcs, vcs, q, lens, w.scale(l),
+                               softcap=softcap)
     return out
 
 
@@ -87,7 +88,8 @@ class GpuRun:
         self.g.gemma_kv_append(self.kc, self.vc, self.w.owner_map, l, d["k_new"], d.get("v_new"),
                                d["write_pos"], k_eq_v=spec.k_eq_v, device_error=self.err)
 
-    def attend(self, l: int, max_seq_len: Optional[int] = None) -> torch.Tensor:
+    def attend(self, l: int, max_seq_len: Optional[int] = None,
+               softcap: Optional[float] = None) -> torch.Tensor:
         w, spec, d = self.w, self.w.layers[l], self.dev[l]
         msl = max(w.ctx_lens) if max_seq_len is None else max_seq_len
         q = d["q"]
@@ -96,10 +98,14 @@ class GpuRun:
         ws_n = self.g.gemma_attn_workspace_size(B, spec.kind, spec.window, spec.n_q, spec.n_kv,
                                                 spec.head_dim, msl, w.n_new)
         ws = torch.zeros(max(ws_n, 1), dtype=torch.uint8, device=q.device)
-        fn = self.g.gemma_attn_decode if w.n_new == 1 else self.g.gemma_attn_prefill
-        fn(out, q, self.kc, self.vc, w.owner_map, l, d["seq_lens"], msl, kind=spec.kind,
-           window=spec.window, n_kv=spec.n_kv, k_eq_v=spec.k_eq_v, scale=w.scale(l),
-           workspace=ws, device_error=self.err)
+        kw = dict(kind=spec.kind, window=spec.window, n_kv=spec.n_kv, k_eq_v=spec.k_eq_v,
+                  scale=w.scale(l), workspace=ws, device_error=self.err)
+        if softcap is not None:
+            self.g.gemma_attn_softcap(out, q, self.kc, self.vc, w.owner_map, l, d["seq_lens"], msl,
+                                      softcap=softcap, **kw)
+        else:
+            fn = self.g.gemma_attn_decode if w.n_new == 1 else self.g.gemma_attn_prefill
+            fn(out, q, self.kc, self.vc, w.owner_map, l, d["seq_lens"], msl, **kw)
         return out
 
     def step(self, layers: Sequence[int]) -> Dict[int, torch.Tensor]:

@@ -75,6 +75,21 @@ def test_decode_argument_errors(kwargs, status):
     assert decode(**kwargs) == status
 
 
+@pytest.mark.parametrize("softcap,status", [(float("nan"), INVALID), (float("inf"), INVALID),
+                                            (-1.0, INVALID)])
+def test_softcap_argument_errors(softcap, status):
+    """The soft-cap entry point rejects a negative or non-finite cap on the host."""
+    st = lib().gemma_attn_softcap(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, 64, 1,
+                                  1, 1, 0, 4, 1, 64, 1, 64, 0.125, softcap, 0, None, 0, None, None)
+    assert st == status
+
+
+def test_softcap_empty_batch_is_ok():
+    assert lib().gemma_attn_softcap(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, 64,
+                                    1, 0, 1, 0, 4, 1, 64, 1, 64, 0.125, 30.0, 0, None, 0, None,
+                                    None) == 0
+
+
 def test_empty_batch_is_ok_without_touching_the_device():
     assert decode(batch=0) == 0
     assert lib().gemma_attn_prefill(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, 64,
