@@ -162,9 +162,9 @@ int gemma_attn_prefill(void* out, const void* q, const void* const* k_cache,
 /*
  * gemma_attn_softcap -- gemma_attn_decode (n_new == 1) or gemma_attn_prefill (n_new > 1) with
  * an attention-logit soft-cap: each scaled score s = scale * q . k becomes
- * softcap * tanh(s / softcap) before the softmax. Source: "Gemma-4 12B on AWS Inferentia2 -
- * Tensor-Parallel (TP=2), device prefill" (the port keeps an explicit attention softcap; the
- * page gives no value, so it is the caller's argument).
+ * softcap * tanh(s / softcap) before the softmax. Source: "Gemma-4-E4B-it on AWS Inferentia2",
+ * Architecture (the recipe keeps an explicit attention softcap; the page gives no value, so it
+ * is the caller's argument).
  *   softcap           finite and >= 0; 0 applies no cap (the call then equals the entry point
  *                     without a cap). Negative or non-finite values return
  *                     GEMMA_ERR_INVALID_ARG.

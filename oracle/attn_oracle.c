@@ -33,11 +33,10 @@
  *    holds len tokens and the i-th of n_tok queries sits at p = len - n_tok + i;
  *  - the softmax scale is an explicit argument (1/sqrt(head_dim) in the
  *    workloads);
- *  - the attention-logit soft-cap ("Gemma-4 12B on AWS Inferentia2 - Tensor-
- *    Parallel (TP=2), device prefill": the port keeps an explicit attention
- *    softcap; no value is given) is optional: with softcap c > 0 each scaled
- *    score s = scale * q.k becomes c * tanh(s / c) before the softmax; c = 0
- *    applies none.
+ *  - the attention-logit soft-cap ("Gemma-4-E4B-it on AWS Inferentia2",
+ *    Architecture: the recipe keeps an explicit attention softcap; no value is
+ *    given) is optional: with softcap c > 0 each scaled score s = scale * q.k
+ *    becomes c * tanh(s / c) before the softmax; c = 0 applies none.
  *
  * Parity pins (tests): torch fp64 scaled_dot_product_attention on tiny shapes,
  * closed forms (uniform weights for K = 0, one-hot V, W = 1, two keys), and
