@@ -38,6 +38,7 @@ import synth  # noqa: E402
 METRIC = "decode-attn HBM GB/s (% of 8 TB/s); prefill-attn bf16 TFLOP/s (% of peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 RAGGED_PHYS_LAYERS = 6   # distinct caches for 48 ragged layer-steps (one 5:1 period)
+SOFTCAP_EXAMPLE = 50.0   # attention-logit soft-cap used to time the soft-capped entry point
 
 # dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
 # captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
@@ -151,9 +152,10 @@ class ClockSampler:
 # device state of a workload (seeded values drawn on the device)
 # ---------------------------------------------------------------------------------------------
 class DeviceState:
-    def __init__(self, w, seed, device, phys_of_layer=None):
+    def __init__(self, w, seed, device, phys_of_layer=None, softcap=None):
         import mixed_sliding_global_gb300 as g
         self.g, self.w, self.device = g, w, device
+        self.softcap = softcap
         gen = torch.Generator(device=device)
         gen.manual_seed(seed)
         self.gen = gen
@@ -201,10 +203,15 @@ class DeviceState:
 
     def layer_call(self, l):
         w, s = self.w, self.w.layers[l]
+        kw = dict(kind=s.kind, window=s.window, n_kv=s.n_kv, k_eq_v=s.k_eq_v, scale=w.scale(l),
+                  workspace=self.ws, device_error=self.err)
+        if self.softcap is not None:
+            self.g.gemma_attn_softcap(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l,
+                                      self.seq_lens, self.max_seq_len, softcap=self.softcap, **kw)
+            return
         fn = self.g.gemma_attn_decode if w.n_new == 1 else self.g.gemma_attn_prefill
         fn(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l, self.seq_lens,
-           self.max_seq_len, kind=s.kind, window=s.window, n_kv=s.n_kv, k_eq_v=s.k_eq_v,
-           scale=w.scale(l), workspace=self.ws, device_error=self.err)
+           self.max_seq_len, **kw)
 
     def append_call(self, l):
         s = self.w.layers[l]
@@ -320,11 +327,12 @@ def workload(name, batch=None, layers=None, offset=0):
     return w, None
 
 
-def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rotations=1):
+def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rotations=1,
+                    softcap=None):
     """Capture one graph per step (rotating over `rotations` independent input copies) and
     time `steps` replays after `warmup` replays. Returns step time and, with per_launch, the
     mean duration of each layer's attention launch over the timed replays."""
-    states = [DeviceState(w, 1234 + 17 * r, device, phys) for r in range(rotations)]
+    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap) for r in range(rotations)]
     for st in states:   # eager pass: sets kernel attributes, checks the error word
         st.step()
     torch.cuda.synchronize()
@@ -481,7 +489,7 @@ def run_native(args):
     scale = 1e9 if decode else 1e12
     work = step_work(w)
     ms, launch_ms, clk, info = timed_graph_run(w, phys, args.steps, args.warmup, device, world,
-                                               per_launch=True)
+                                               per_launch=True, softcap=args.softcap)
     ms = max_over_ranks(ms, world)
     value = job_value(work, world, ms, scale)
 
@@ -537,7 +545,8 @@ def run_native(args):
                        "parallelism": f"dp{world}" if world > 1 else "single",
                        "l2": "inputs larger than L2 (each layer-step reads > 129 MB)"
                        if args.workload == "ragged_decode" else "inputs larger than L2",
-                       "phys_caches": len(set(phys)) if phys else w.n_layers},
+                       "phys_caches": len(set(phys)) if phys else w.n_layers,
+                       **({"softcap": args.softcap} if args.softcap is not None else {})},
             "roofline": roof,
             "gpu_launches": info["launches_per_step"] * args.steps,
             "clocks": clk}
@@ -553,12 +562,16 @@ def run_native(args):
                                     "kind": "oracle", "sample": desc}
         # the other benchmark configurations, same contract, reported alongside
         also = {}
-        for name in [n for n in ("prefill", "12b_decode", "e4b_decode") if n != args.workload]:
-            w2, phys2 = workload(name)
+        # prefill_softcap: the prefill bucket through the soft-capped entry point (cap 50, an
+        # example value: the pages name an attention soft-cap without its value)
+        for name in [n for n in ("prefill", "prefill_softcap", "12b_decode", "e4b_decode")
+                     if n != args.workload]:
+            cap2 = SOFTCAP_EXAMPLE if name == "prefill_softcap" else None
+            w2, phys2 = workload("prefill" if name == "prefill_softcap" else name)
             rot = 12 if name == "e4b_decode" else 1   # e4b inputs (32 MB) rotate past L2
             ms2, lm2, clk2, info2 = timed_graph_run(w2, phys2, args.steps, args.warmup, device,
-                                                    world, per_launch=(name == "prefill"),
-                                                    rotations=rot)
+                                                    world, per_launch=(w2.n_new > 1),
+                                                    rotations=rot, softcap=cap2)
             ms2 = max_over_ranks(ms2, world)
             d2 = w2.n_new == 1
             u2, sc2 = ("GB/s", 1e9) if d2 else ("TFLOP/s", 1e12)
@@ -582,6 +595,8 @@ def run_native(args):
                                            "launch_us": 1e3 * t / len(ls)}
             if rot > 1:
                 ent["l2"] = f"{rot} rotating input copies"
+            if cap2 is not None:
+                ent["softcap"] = cap2
             also[name] = ent
         line["also"] = also
     if rank == 0:
@@ -605,6 +620,8 @@ def main():
                     help="fewer ragged layer-steps (profiling captures only; not a bench line)")
     ap.add_argument("--layer-offset", type=int, default=0,
                     help="first ragged layer (profiling captures only; not a bench line)")
+    ap.add_argument("--softcap", type=float, default=None,
+                    help="time the workload through the soft-capped entry point with this cap")
     ap.add_argument("--quick", action="store_true",
                     help="main workload only (no e2e, CPU baseline or other configurations)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,

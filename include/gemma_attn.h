@@ -65,6 +65,7 @@ typedef enum {
 #define GEMMA_DEVERR_SEQ_LEN 1u    /* seq_lens[b] outside [n_tok, min(kv_capacity, max_seq_len)] */
 #define GEMMA_DEVERR_WRITE_POS 2u  /* write_pos[b] < 0 or write_pos[b] + n_new > kv_capacity */
 #define GEMMA_DEVERR_TIMEOUT 4u    /* an internal pipeline wait gave up */
+#define GEMMA_DEVERR_N_REAL 8u     /* n_real[b] outside [0, n_new] (padded-bucket entry points) */
 
 /*
  * gemma_kv_append -- write this step's new K (and V) rows of an owner layer into its cache.
@@ -178,6 +179,36 @@ int gemma_attn_softcap(void* out, const void* q, const void* const* k_cache,
                        int head_dim, int k_eq_v, int kv_capacity, float scale, float softcap,
                        gemma_dtype dtype, void* workspace, size_t workspace_bytes,
                        uint32_t* device_error, void* stream);
+
+/*
+ * gemma_kv_append_bucket / gemma_attn_prefill_bucket -- the padded prefill bucket: every
+ * sequence brings n_new query rows (and n_new new K/V rows), of which only the first
+ * n_real[b] are real tokens; the rest pad the sequence to the bucket size. Source: first page,
+ * section 5.1 ("prefill (padded prompt <= KV_BUCKET ...)") and the 12B model card (prefill
+ * bucket of seq = 64); the pages pad and trace a fixed shape, here the pad rows are masked
+ * exactly: they are neither written to the cache nor attended, and their outputs are zero.
+ *   n_real            DEVICE int32[batch], 0 <= n_real[b] <= n_new (else the sequence is
+ *                     skipped and GEMMA_DEVERR_N_REAL is reported).
+ *   gemma_kv_append_bucket writes rows t < n_real[b] at write_pos[b] + t; other arguments as
+ *   for gemma_kv_append.
+ *   gemma_attn_prefill_bucket: seq_lens[b] counts the real tokens only (n_real[b] <=
+ *   seq_lens[b]); the i-th real token of sequence b sits at seq_lens[b] - n_real[b] + i and
+ *   attends as in gemma_attn_prefill. Other arguments and the workspace as for
+ *   gemma_attn_prefill (n_new == 1 is allowed).
+ */
+int gemma_kv_append_bucket(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
+                           int n_layers, int layer, const void* k_new, const void* v_new,
+                           const int32_t* write_pos, const int32_t* n_real, int batch, int n_new,
+                           int n_kv, int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
+                           uint32_t* device_error, void* stream);
+
+int gemma_attn_prefill_bucket(void* out, const void* q, const void* const* k_cache,
+                              const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                              int layer, const int32_t* seq_lens, const int32_t* n_real,
+                              int max_seq_len, int n_new, int batch, gemma_layer_kind kind,
+                              int window, int n_q, int n_kv, int head_dim, int k_eq_v,
+                              int kv_capacity, float scale, gemma_dtype dtype, void* workspace,
+                              size_t workspace_bytes, uint32_t* device_error, void* stream);
 
 /*
  * gemma_attn_workspace_size -- bytes of scratch that gemma_attn_decode (n_new == 1) or

@@ -14,6 +14,7 @@ GEMMA_SLIDING, GEMMA_GLOBAL = 0, 1
 GEMMA_BF16, GEMMA_FP32 = 0, 1
 GEMMA_OK = 0
 GEMMA_DEVERR_SEQ_LEN, GEMMA_DEVERR_WRITE_POS, GEMMA_DEVERR_TIMEOUT = 1, 2, 4
+GEMMA_DEVERR_N_REAL = 8
 
 _c_int, _c_void_p, _c_size_t, _c_float = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
 _PVOID = ctypes.POINTER(ctypes.c_void_p)
@@ -39,6 +40,14 @@ _SIGNATURES = {
                                     _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     _c_int, _c_int, _c_int, _c_int, _c_float, _c_float, _c_int,
                                     _c_void_p, _c_size_t, _c_void_p, _c_void_p]),
+    "gemma_kv_append_bucket": (_c_int, [_PVOID, _PVOID, _PI32, _c_int, _c_int, _c_void_p,
+                                        _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                        _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_void_p]),
+    "gemma_attn_prefill_bucket": (_c_int, [_c_void_p, _c_void_p, _PVOID, _PVOID, _PI32, _c_int,
+                                           _c_int, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                           _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                           _c_int, _c_float, _c_int, _c_void_p, _c_size_t,
+                                           _c_void_p, _c_void_p]),
     "gemma_attn_workspace_size": (_c_size_t, [_c_int] * 8),
     "gemma_status_string": (ctypes.c_char_p, [_c_int]),
     "gemma_abi_version": (_c_int, []),
@@ -149,6 +158,50 @@ def gemma_kv_append(k_cache: Sequence[Optional[torch.Tensor]],
         _dev_ptr(k_new), _dev_ptr(v_new), _dev_ptr(write_pos), B, n_new, n_kv, d, cap,
         int(bool(k_eq_v)), _dtype(k_new), _dev_ptr(device_error), _stream(stream))
     _check("gemma_kv_append", st)
+
+
+def gemma_kv_append_bucket(k_cache: Sequence[Optional[torch.Tensor]],
+                           v_cache: Optional[Sequence[Optional[torch.Tensor]]],
+                           owner_map: Sequence[int], layer: int, k_new: torch.Tensor,
+                           v_new: Optional[torch.Tensor], write_pos: torch.Tensor,
+                           n_real: torch.Tensor, *, k_eq_v: bool, kv_capacity: Optional[int] = None,
+                           device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """gemma_kv_append for a padded bucket: only rows t < n_real[b] (int32 [B]) are written."""
+    B, n_new, n_kv, d = k_new.shape
+    n_layers = len(owner_map)
+    kc = k_cache[int(owner_map[layer])]
+    cap = kv_capacity if kv_capacity is not None else (kc.shape[2] if kc is not None else 0)
+    vcs = list(v_cache) if v_cache is not None else [None] * n_layers
+    st = library().gemma_kv_append_bucket(
+        _ptr_array(list(k_cache)), _ptr_array(vcs), _i32_array(owner_map), n_layers, layer,
+        _dev_ptr(k_new), _dev_ptr(v_new), _dev_ptr(write_pos), _dev_ptr(n_real), B, n_new, n_kv,
+        d, cap, int(bool(k_eq_v)), _dtype(k_new), _dev_ptr(device_error), _stream(stream))
+    _check("gemma_kv_append_bucket", st)
+
+
+def gemma_attn_prefill_bucket(out: torch.Tensor, q: torch.Tensor, k_cache, v_cache, owner_map,
+                              layer: int, seq_lens: torch.Tensor, n_real: torch.Tensor,
+                              max_seq_len: int, *, kind: int, window: int, n_kv: int,
+                              k_eq_v: bool, scale: float, kv_capacity: Optional[int] = None,
+                              workspace: Optional[torch.Tensor] = None,
+                              device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Prefill of a padded bucket: q, out [B][n_new][n_q][d], the first n_real[b] rows real;
+    pad rows' outputs are zero."""
+    B, n_new = q.shape[0], q.shape[1]
+    n_q, d = q.shape[-2], q.shape[-1]
+    n_layers = len(owner_map)
+    kc = _cache_of(k_cache, owner_map, layer)
+    cap = kv_capacity if kv_capacity is not None else kc.shape[2]
+    vcs = list(v_cache) if v_cache is not None else [None] * n_layers
+    ws_ptr = _dev_ptr(workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = library().gemma_attn_prefill_bucket(
+        _dev_ptr(out), _dev_ptr(q), _ptr_array(list(k_cache)), _ptr_array(vcs),
+        _i32_array(owner_map), n_layers, layer, _dev_ptr(seq_lens), _dev_ptr(n_real),
+        int(max_seq_len), n_new, B, int(kind), int(window), n_q, int(n_kv), d,
+        int(bool(k_eq_v)), int(cap), float(scale), _dtype(q), ws_ptr, ws_bytes,
+        _dev_ptr(device_error), _stream(stream))
+    _check("gemma_attn_prefill_bucket", st)
 
 
 def gemma_attn_workspace_size(batch: int, kind: int, window: int, n_q: int, n_kv: int,

@@ -99,7 +99,8 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
               const int32_t* owner_map, int n_layers, int layer, const int32_t* seq_lens,
               int max_seq_len, int n_tok, int batch, int kind, int window, int n_q, int n_kv,
               int head_dim, int k_eq_v, int kv_capacity, float scale, float softcap, int dtype,
-              void* workspace, size_t workspace_bytes, uint32_t* device_error, void* stream) {
+              void* workspace, size_t workspace_bytes, uint32_t* device_error, void* stream,
+              const int32_t* n_real = nullptr) {
     if (batch < 0 || n_tok < 1) return GEMMA_ERR_INVALID_ARG;
     if (!std::isfinite(softcap) || softcap < 0.f) return GEMMA_ERR_INVALID_ARG;
     int st = check_shape(kind, window, n_q, n_kv, head_dim, dtype);
@@ -123,7 +124,10 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
         return GEMMA_ERR_INVALID_ARG;
     const int n_sm = sm_count();
     if (n_sm < 0) return GEMMA_ERR_CUDA;
-    const Plan pl = make_plan(batch, kind, window, n_q, n_kv, head_dim, max_seq_len, n_tok, n_sm);
+    // a padded bucket is never split over keys (pad rows have no key range to merge)
+    const Plan pl = n_real ? Plan{1, 1 << 30, 0, 0}
+                           : make_plan(batch, kind, window, n_q, n_kv, head_dim, max_seq_len,
+                                       n_tok, n_sm);
     if (pl.ws_bytes > 0 &&
         (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace)))
         return GEMMA_ERR_WORKSPACE;
@@ -133,6 +137,7 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     p.k = kc;
     p.v = vc;
     p.seq_lens = seq_lens;
+    p.n_real = n_real;
     p.out = out;
     p.o_part = pl.ws_bytes ? static_cast<float*>(workspace) : nullptr;
     p.ml_part = pl.ws_bytes
@@ -158,7 +163,7 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const long long rows = (long long)n_tok * p.G;
     cudaError_t e;
-    if (dtype == GEMMA_BF16 && n_tok > 1 && gemma::prefill_tc_supported(head_dim)) {
+    if (dtype == GEMMA_BF16 && (n_tok > 1 || n_real) && gemma::prefill_tc_supported(head_dim)) {
         e = gemma::launch_prefill_tc(p, head_dim, batch, s);
     } else if (dtype == GEMMA_BF16) {
         const size_t smem = gemma::rows_bf16_smem_bytes(head_dim, p.k_eq_v, &p.n_stages);
@@ -174,6 +179,12 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
         e = gemma::launch_combine(p, head_dim, batch, dtype == GEMMA_FP32, s);
     return e == cudaSuccess ? GEMMA_OK : GEMMA_ERR_CUDA;
 }
+
+int append_rows(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
+                int n_layers, int layer, const void* k_new, const void* v_new,
+                const int32_t* write_pos, const int32_t* n_real, int batch, int n_new, int n_kv,
+                int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
+                uint32_t* device_error, void* stream);
 
 }  // namespace
 
@@ -198,6 +209,31 @@ int gemma_kv_append(void* const* k_cache, void* const* v_cache, const int32_t* o
                     const int32_t* write_pos, int batch, int n_new, int n_kv, int head_dim,
                     int kv_capacity, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
                     void* stream) {
+    return append_rows(k_cache, v_cache, owner_map, n_layers, layer, k_new, v_new, write_pos,
+                       nullptr, batch, n_new, n_kv, head_dim, kv_capacity, k_eq_v, dtype,
+                       device_error, stream);
+}
+
+int gemma_kv_append_bucket(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
+                           int n_layers, int layer, const void* k_new, const void* v_new,
+                           const int32_t* write_pos, const int32_t* n_real, int batch, int n_new,
+                           int n_kv, int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
+                           uint32_t* device_error, void* stream) {
+    if (!n_real && batch > 0 && n_new > 0) return GEMMA_ERR_INVALID_ARG;
+    return append_rows(k_cache, v_cache, owner_map, n_layers, layer, k_new, v_new, write_pos,
+                       n_real, batch, n_new, n_kv, head_dim, kv_capacity, k_eq_v, dtype,
+                       device_error, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int append_rows(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
+                int n_layers, int layer, const void* k_new, const void* v_new,
+                const int32_t* write_pos, const int32_t* n_real, int batch, int n_new, int n_kv,
+                int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
+                uint32_t* device_error, void* stream) {
     if (batch < 0 || n_new < 0 || n_kv < 1 || kv_capacity < 1) return GEMMA_ERR_INVALID_ARG;
     if (dtype != GEMMA_BF16 && dtype != GEMMA_FP32) return GEMMA_ERR_INVALID_ARG;
     if (!head_dim_ok(head_dim)) return GEMMA_ERR_UNSUPPORTED;
@@ -220,10 +256,15 @@ int gemma_kv_append(void* const* k_cache, void* const* v_cache, const int32_t* o
     if (n_sm < 0) return GEMMA_ERR_CUDA;
     const int row_bytes = head_dim * (dtype == GEMMA_BF16 ? 2 : 4);
     cudaError_t e = gemma::launch_kv_append(k_cache[layer], vc, k_new, vc ? v_new : nullptr,
-                                            write_pos, batch, n_new, n_kv, kv_capacity, row_bytes,
-                                            device_error, n_sm, static_cast<cudaStream_t>(stream));
+                                            write_pos, n_real, batch, n_new, n_kv, kv_capacity,
+                                            row_bytes, device_error, n_sm,
+                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GEMMA_OK : GEMMA_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
 
 int gemma_attn_decode(void* out, const void* q, const void* const* k_cache,
                       const void* const* v_cache, const int32_t* owner_map, int n_layers,
@@ -261,6 +302,20 @@ int gemma_attn_softcap(void* out, const void* q, const void* const* k_cache,
     return attention(out, q, k_cache, v_cache, owner_map, n_layers, layer, seq_lens, max_seq_len,
                      n_new, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
                      softcap, dtype, workspace, workspace_bytes, device_error, stream);
+}
+
+int gemma_attn_prefill_bucket(void* out, const void* q, const void* const* k_cache,
+                              const void* const* v_cache, const int32_t* owner_map, int n_layers,
+                              int layer, const int32_t* seq_lens, const int32_t* n_real,
+                              int max_seq_len, int n_new, int batch, gemma_layer_kind kind,
+                              int window, int n_q, int n_kv, int head_dim, int k_eq_v,
+                              int kv_capacity, float scale, gemma_dtype dtype, void* workspace,
+                              size_t workspace_bytes, uint32_t* device_error, void* stream) {
+    if (n_new == 0 && batch >= 0) return GEMMA_OK;
+    if (!n_real && batch > 0) return GEMMA_ERR_INVALID_ARG;
+    return attention(out, q, k_cache, v_cache, owner_map, n_layers, layer, seq_lens, max_seq_len,
+                     n_new, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
+                     0.f, dtype, workspace, workspace_bytes, device_error, stream, n_real);
 }
 
 size_t gemma_attn_workspace_size(int batch, gemma_layer_kind kind, int window, int n_q,

@@ -16,6 +16,7 @@ struct RowsParams {
     const void* k;            // owner layer's K cache [B][n_kv][cap][D]
     const void* v;            // owner layer's V cache (== k when k_eq_v)
     const int32_t* seq_lens;  // [B], tokens in the cache after this step's append
+    const int32_t* n_real;    // [B] real tokens of a padded prefill bucket, or nullptr (all real)
     void* out;                // [B][n_tok][n_q][D], written when n_split == 1
     float* o_part;            // [B][n_q][n_split][D]  unnormalised partial outputs
     float* ml_part;           // [B][n_q][n_split][2]  (running max in log2 units, sum)
@@ -49,7 +50,8 @@ cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out
 bool prefill_tc_supported(int head_dim);
 cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cudaStream_t st);
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
-                             const int32_t* write_pos, int batch, int n_new, int n_kv,
+                             const int32_t* write_pos, const int32_t* n_real, int batch,
+                             int n_new, int n_kv,
                              int capacity, int row_bytes, uint32_t* err, int n_sm,
                              cudaStream_t st);
 

@@ -1,6 +1,7 @@
 // kv_append.cu -- in-place write of this step's new K/V rows into an owner layer's cache.
 //
-//   cache[b][h][write_pos[b] + t][:] = new[b][t][h][:]
+//   cache[b][h][write_pos[b] + t][:] = new[b][t][h][:]     for t < n_real[b] (all n_new rows
+//                                                           when n_real is null)
 //
 // "Gemma-4-E4B-it on AWS Inferentia2" ("Decode neff") keeps the KV buffers on the device and
 // updates them in place each step; its one-hot masked write exists only to keep a traced
@@ -17,6 +18,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
                                                         const uint8_t* __restrict__ kn,
                                                         const uint8_t* __restrict__ vn,
                                                         const int32_t* __restrict__ write_pos,
+                                                        const int32_t* __restrict__ n_real,
                                                         int batch, int n_new, int n_kv,
                                                         int capacity, int row_bytes,
                                                         uint32_t* err) {
@@ -31,7 +33,13 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
         const int t = (int)(bt % n_new);
         const int b = (int)(bt / n_new);
         const int pos = __ldg(write_pos + b);
-        if (pos < 0 || (long long)pos + n_new > capacity) {
+        const int nr = n_real ? __ldg(n_real + b) : n_new;  // rows of this sequence to write
+        if (nr < 0 || nr > n_new) {
+            if (t == 0 && h == 0 && ch == 0) report(err, GEMMA_DEVERR_N_REAL);
+            continue;
+        }
+        if (t >= nr) continue;  // a pad row of a padded bucket
+        if (pos < 0 || (long long)pos + nr > capacity) {
             if (t == 0 && h == 0 && ch == 0) report(err, GEMMA_DEVERR_WRITE_POS);
             continue;
         }
@@ -44,9 +52,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
 }
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
-                             const int32_t* write_pos, int batch, int n_new, int n_kv,
-                             int capacity, int row_bytes, uint32_t* err, int n_sm,
-                             cudaStream_t st) {
+                             const int32_t* write_pos, const int32_t* n_real, int batch,
+                             int n_new, int n_kv, int capacity, int row_bytes, uint32_t* err,
+                             int n_sm, cudaStream_t st) {
     const long long total = (long long)batch * n_new * n_kv * (row_bytes / 16);
     long long blocks = (total + 255) / 256;
     const long long cap_blocks = (long long)n_sm * 8;
@@ -54,8 +62,8 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, co
     if (blocks < 1) blocks = 1;
     kv_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(
         static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
-        static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), write_pos, batch,
-        n_new, n_kv, capacity, row_bytes, err);
+        static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), write_pos, n_real,
+        batch, n_new, n_kv, capacity, row_bytes, err);
     return cudaGetLastError();
 }
 

@@ -159,16 +159,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int rt = blockIdx.x / CL, kvh = blockIdx.y, b = blockIdx.z;
     const int rows_total = p.n_tok * p.G;
     const int row0 = rt * 128;
-    const int n_rows = min(128, rows_total - row0);
+    const int n_rows = min(128, rows_total - row0);  // rows of the bucket this CTA writes
     const int len = __ldg(p.seq_lens + b);
-    const bool bad = len < p.n_tok || len > p.cap || len > p.max_seq_len;
+    // real tokens of this sequence (a padded bucket's first n_real rows; all rows otherwise);
+    // the i-th real token sits at len - n_real + i, the pad rows' outputs are zero
+    const int n_real = p.n_real ? __ldg(p.n_real + b) : p.n_tok;
+    const bool bad_real = n_real < 0 || n_real > p.n_tok;
+    const bool bad = bad_real || len < n_real || len > p.cap || len > p.max_seq_len;
+    const int n_rows_real = bad ? 0 : max(0, min(128, n_real * p.G - row0));  // rows that attend
 
-    // key range of the tile: from the first row's window start to the last row's position
-    const int tok_first = row0 / p.G, tok_last = (row0 + n_rows - 1) / p.G;
-    const int pos_first = len - p.n_tok + tok_first, pos_last = len - p.n_tok + tok_last;
+    // key range of the tile: from the first row's window start to the last real row's position
+    const int tok_first = row0 / p.G, tok_last = (row0 + max(n_rows_real, 1) - 1) / p.G;
+    const int pos_first = len - n_real + tok_first, pos_last = len - n_real + tok_last;
     const int k_begin = p.is_sliding ? max(0, pos_first - p.window + 1) : 0;
     const int k_end = pos_last + 1;
-    const int n_tiles = bad ? 0 : (k_end - k_begin + kTcKeys - 1) / kTcKeys;
+    const int n_tiles = n_rows_real == 0 ? 0 : (k_end - k_begin + kTcKeys - 1) / kTcKeys;
     // K/V ring split: with K = V one ring of NS slots; otherwise NV slots for V (V is needed
     // only by P V, which comes last) and the rest for K
     const int NV = p.k_eq_v ? 0 : (NS / 3 > 1 ? NS / 3 : 1);
@@ -326,13 +331,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------ softmax warps --------------------------------------
         const int r = threadIdx.x;  // tile row = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        const bool row_ok = !bad && r < n_rows;
+        const bool row_ok = r < n_rows_real;
         int token = 0, head = 0, lo = 1, hi = 0;
         if (row_ok) {
             const int R = row0 + r;
             token = R / p.G;
             head = kvh * p.G + (R - token * p.G);
-            const int pos = len - p.n_tok + token;
+            const int pos = len - n_real + token;
             lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
             hi = pos + 1;
         }
@@ -518,7 +523,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         }
-        if (bad && r == 0 && kvh == 0 && rt == 0 && h == 0) report(p.err, GEMMA_DEVERR_SEQ_LEN);
+        if (bad && r == 0 && kvh == 0 && rt == 0 && h == 0)
+            report(p.err, bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
     }
     tc_fence_before();
     __syncthreads();

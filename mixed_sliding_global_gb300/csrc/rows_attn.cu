@@ -402,15 +402,19 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
     const int token = R / p.G, head = kvh * p.G + (R - token * p.G);
     float* out_row = reinterpret_cast<float*>(p.out) +
                      (((size_t)b * p.n_tok + token) * p.n_q + head) * (size_t)D;
-    if (len < p.n_tok || len > p.cap || len > p.max_seq_len) {
+    // real tokens of this sequence (a padded bucket's first n_real rows; all rows otherwise)
+    const int n_real = p.n_real ? __ldg(p.n_real + b) : p.n_tok;
+    const bool bad_real = n_real < 0 || n_real > p.n_tok;
+    const bool bad = bad_real || len < n_real || len > p.cap || len > p.max_seq_len;
+    if (bad || token >= n_real) {  // a bad sequence, or a pad row: zero output
         if (split == 0) {
-            if (lane == 0) report(p.err, GEMMA_DEVERR_SEQ_LEN);
+            if (bad && lane == 0) report(p.err, bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
             if (direct)
                 for (int e = 0; e < E; ++e) out_row[lane + 32 * e] = 0.f;
         }
         return;
     }
-    const int pos = len - p.n_tok + token;
+    const int pos = len - n_real + token;
     const int lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
     const int kb = lo + split * p.chunk;
     const int ke = min(pos + 1, kb + p.chunk);

@@ -90,6 +90,18 @@ def test_softcap_empty_batch_is_ok():
                                     None) == 0
 
 
+def test_bucket_entry_points_need_n_real():
+    """The padded-bucket entry points reject a missing n_real array on the host."""
+    assert lib().gemma_kv_append_bucket(_ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, None, FAKE,
+                                        None, 1, 4, 1, 64, 64, 1, 0, None, None) == INVALID
+    assert lib().gemma_attn_prefill_bucket(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0,
+                                           FAKE, None, 64, 4, 1, 1, 0, 4, 1, 64, 1, 64, 0.125, 0,
+                                           None, 0, None, None) == INVALID
+    assert lib().gemma_attn_prefill_bucket(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0,
+                                           FAKE, FAKE, 64, 4, 0, 1, 0, 4, 1, 64, 1, 64, 0.125, 0,
+                                           None, 0, None, None) == 0   # empty batch
+
+
 def test_empty_batch_is_ok_without_touching_the_device():
     assert decode(batch=0) == 0
     assert lib().gemma_attn_prefill(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, 64,
