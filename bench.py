@@ -39,6 +39,7 @@ METRIC = "decode-attn HBM GB/s (% of 8 TB/s); prefill-attn bf16 TFLOP/s (% of pe
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 RAGGED_PHYS_LAYERS = 6   # distinct caches for 48 ragged layer-steps (one 5:1 period)
 SOFTCAP_EXAMPLE = 50.0   # attention-logit soft-cap used to time the soft-capped entry point
+BUCKET_REAL_EXAMPLE = [512, 384, 256, 128]   # real rows per sequence of the padded bucket timed
 
 # dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
 # captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
@@ -68,21 +69,22 @@ def append_bytes(w, l):
     return 2 * w.batch * w.n_new * s.n_kv * s.head_dim * 2 * (1 if s.k_eq_v else 2)
 
 
-def prefill_flops(w, l):
-    """4 d n_q per attended (query, key) pair: QK^T and PV multiply-adds."""
+def prefill_flops(w, l, n_real=None):
+    """4 d n_q per attended (query, key) pair: QK^T and PV multiply-adds (real rows only for a
+    padded bucket: they sit where the bucket's first n_real rows would)."""
     s = w.layers[l]
     pairs = 0
-    for c in w.ctx_lens:
-        for i in range(w.n_new):
+    for b, c in enumerate(w.ctx_lens):
+        for i in range(w.n_new if n_real is None else n_real[b]):
             p = c - w.n_new + i
             pairs += min(p + 1, s.window) if s.kind == synth.SLIDING else p + 1
     return 4 * s.head_dim * s.n_q * pairs
 
 
-def step_work(w):
+def step_work(w, n_real=None):
     if w.n_new == 1:
         return sum(decode_bytes(w, l) + append_bytes(w, l) for l in range(w.n_layers))
-    return sum(prefill_flops(w, l) for l in range(w.n_layers))
+    return sum(prefill_flops(w, l, n_real) for l in range(w.n_layers))
 
 
 def load_peaks():
@@ -152,18 +154,22 @@ class ClockSampler:
 # device state of a workload (seeded values drawn on the device)
 # ---------------------------------------------------------------------------------------------
 class DeviceState:
-    def __init__(self, w, seed, device, phys_of_layer=None, softcap=None):
+    def __init__(self, w, seed, device, phys_of_layer=None, softcap=None, n_real=None):
         import mixed_sliding_global_gb300 as g
         self.g, self.w, self.device = g, w, device
         self.softcap = softcap
+        # padded prefill bucket: real rows per sequence (the rest pad the bucket to n_new)
+        self.n_real = None if n_real is None else torch.tensor(n_real, dtype=torch.int32,
+                                                                device=device)
         gen = torch.Generator(device=device)
         gen.manual_seed(seed)
         self.gen = gen
         n, B, cap = w.n_layers, w.batch, w.capacity
         phys = phys_of_layer or list(range(n))
         ctx = torch.tensor(w.ctx_lens, dtype=torch.int32)
-        self.seq_lens = ctx.to(device)
         self.write_pos = (ctx - w.n_new).to(device)
+        self.seq_lens = ctx.to(device) if n_real is None else \
+            (ctx - w.n_new + torch.tensor(n_real, dtype=torch.int32)).to(device)
         kc_phys, vc_phys = {}, {}
         self.kc, self.vc = [None] * n, [None] * n
         self.q, self.k_new, self.v_new, self.out = [None] * n, [None] * n, [None] * n, [None] * n
@@ -209,12 +215,22 @@ class DeviceState:
             self.g.gemma_attn_softcap(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l,
                                       self.seq_lens, self.max_seq_len, softcap=self.softcap, **kw)
             return
+        if self.n_real is not None:
+            self.g.gemma_attn_prefill_bucket(self.out[l], self.q[l], self.kc, self.vc,
+                                             w.owner_map, l, self.seq_lens, self.n_real,
+                                             self.max_seq_len, **kw)
+            return
         fn = self.g.gemma_attn_decode if w.n_new == 1 else self.g.gemma_attn_prefill
         fn(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l, self.seq_lens,
            self.max_seq_len, **kw)
 
     def append_call(self, l):
         s = self.w.layers[l]
+        if self.n_real is not None:
+            self.g.gemma_kv_append_bucket(self.kc, self.vc, self.w.owner_map, l, self.k_new[l],
+                                          self.v_new[l], self.write_pos, self.n_real,
+                                          k_eq_v=s.k_eq_v, device_error=self.err)
+            return
         self.g.gemma_kv_append(self.kc, self.vc, self.w.owner_map, l, self.k_new[l],
                                self.v_new[l], self.write_pos, k_eq_v=s.k_eq_v,
                                device_error=self.err)
@@ -328,11 +344,12 @@ def workload(name, batch=None, layers=None, offset=0):
 
 
 def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rotations=1,
-                    softcap=None):
+                    softcap=None, n_real=None):
     """Capture one graph per step (rotating over `rotations` independent input copies) and
     time `steps` replays after `warmup` replays. Returns step time and, with per_launch, the
     mean duration of each layer's attention launch over the timed replays."""
-    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap) for r in range(rotations)]
+    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap, n_real)
+              for r in range(rotations)]
     for st in states:   # eager pass: sets kernel attributes, checks the error word
         st.step()
     torch.cuda.synchronize()
@@ -564,32 +581,36 @@ def run_native(args):
         also = {}
         # prefill_softcap: the prefill bucket through the soft-capped entry point (cap 50, an
         # example value: the pages name an attention soft-cap without its value)
-        for name in [n for n in ("prefill", "prefill_softcap", "12b_decode", "e4b_decode")
-                     if n != args.workload]:
+        # prefill_bucket: the prefill bucket padded, real lengths 512/384/256/128 of 512 (the
+        # TFLOP/s count the real rows' work only)
+        for name in [n for n in ("prefill", "prefill_softcap", "prefill_bucket", "12b_decode",
+                                 "e4b_decode") if n != args.workload]:
             cap2 = SOFTCAP_EXAMPLE if name == "prefill_softcap" else None
-            w2, phys2 = workload("prefill" if name == "prefill_softcap" else name)
+            real2 = BUCKET_REAL_EXAMPLE if name == "prefill_bucket" else None
+            w2, phys2 = workload("prefill" if name.startswith("prefill") else name)
             rot = 12 if name == "e4b_decode" else 1   # e4b inputs (32 MB) rotate past L2
             ms2, lm2, clk2, info2 = timed_graph_run(w2, phys2, args.steps, args.warmup, device,
                                                     world, per_launch=(w2.n_new > 1),
-                                                    rotations=rot, softcap=cap2)
+                                                    rotations=rot, softcap=cap2, n_real=real2)
             ms2 = max_over_ranks(ms2, world)
             d2 = w2.n_new == 1
             u2, sc2 = ("GB/s", 1e9) if d2 else ("TFLOP/s", 1e12)
-            v2 = world * step_work(w2) / (ms2 * 1e-3) / sc2
+            v2 = world * step_work(w2, real2) / (ms2 * 1e-3) / sc2
             ent = {"value": v2, "unit": u2, "ms_per_step": ms2,
                    "frac": v2 / (peaks["hbm_gbs"] if d2 else peaks["bf16_tflops_sustained"]),
                    "us_per_layer_step": 1e3 * ms2 / w2.n_layers,
                    "gpu_launches_per_step": info2["launches_per_step"],
                    "clocks": clk2}
             if lm2 is not None:
-                ach = sum(prefill_flops(w2, l) for l in range(w2.n_layers)) / (sum(lm2) * 1e-3) / 1e12
+                ach = sum(prefill_flops(w2, l, real2) for l in range(w2.n_layers)) / \
+                    (sum(lm2) * 1e-3) / 1e12
                 ent["roofline"] = {"bound": "tensor", "achieved": ach,
                                    "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                                    "frac": ach / peaks["bf16_tflops_sustained"],
                                    "peak_source": peak_src + " sustained"}
                 for kind, nm in ((synth.SLIDING, "sliding"), (synth.GLOBAL, "global")):
                     ls = [l for l, s in enumerate(w2.layers) if s.kind == kind]
-                    f = sum(prefill_flops(w2, l) for l in ls)
+                    f = sum(prefill_flops(w2, l, real2) for l in ls)
                     t = sum(lm2[l] for l in ls)
                     ent["roofline"][nm] = {"tflops": f / (t * 1e-3) / 1e12,
                                            "launch_us": 1e3 * t / len(ls)}
@@ -597,6 +618,8 @@ def run_native(args):
                 ent["l2"] = f"{rot} rotating input copies"
             if cap2 is not None:
                 ent["softcap"] = cap2
+            if real2 is not None:
+                ent["n_real"] = real2
             also[name] = ent
         line["also"] = also
     if rank == 0:
