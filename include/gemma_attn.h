@@ -181,6 +181,30 @@ int gemma_attn_softcap(void* out, const void* q, const void* const* k_cache,
                        uint32_t* device_error, void* stream);
 
 /*
+ * gemma_attn_decode_append -- gemma_kv_append followed by gemma_attn_decode, in one launch:
+ * the CTA of the decode kernel whose key chunk holds write_pos[b] writes this step's K (and V)
+ * row of its KV head into the cache before it loads that chunk, so the step needs no separate
+ * append launch. Source: first page, section 5.1 and the E4B model card ("Decode neff": the KV
+ * buffers are updated in place inside the decode step itself).
+ *   k_cache, v_cache  as for gemma_kv_append (written) and gemma_attn_decode (read).
+ *   k_new, v_new      DEVICE [batch][1][n_kv][head_dim]; ignored on a shared layer (which
+ *                     then runs gemma_attn_decode against its owner's cache).
+ *   write_pos         DEVICE int32[batch]; normally seq_lens[b] - 1. A slot outside
+ *                     [0, kv_capacity) is reported (GEMMA_DEVERR_WRITE_POS) and not written;
+ *                     a sequence whose seq_lens[b] is invalid is skipped entirely.
+ *   Other arguments, the workspace and the results as for gemma_attn_decode. The fp32 debug
+ *   path runs the append and the decode as two launches.
+ */
+int gemma_attn_decode_append(void* out, const void* q, void* const* k_cache, void* const* v_cache,
+                             const int32_t* owner_map, int n_layers, int layer, const void* k_new,
+                             const void* v_new, const int32_t* write_pos,
+                             const int32_t* seq_lens, int max_seq_len, int batch,
+                             gemma_layer_kind kind, int window, int n_q, int n_kv, int head_dim,
+                             int k_eq_v, int kv_capacity, float scale, gemma_dtype dtype,
+                             void* workspace, size_t workspace_bytes, uint32_t* device_error,
+                             void* stream);
+
+/*
  * gemma_kv_append_bucket / gemma_attn_prefill_bucket -- the padded prefill bucket: every
  * sequence brings n_new query rows (and n_new new K/V rows), of which only the first
  * n_real[b] are real tokens; the rest pad the sequence to the bucket size. Source: first page,

@@ -40,6 +40,11 @@ _SIGNATURES = {
                                     _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     _c_int, _c_int, _c_int, _c_int, _c_float, _c_float, _c_int,
                                     _c_void_p, _c_size_t, _c_void_p, _c_void_p]),
+    "gemma_attn_decode_append": (_c_int, [_c_void_p, _c_void_p, _PVOID, _PVOID, _PI32, _c_int,
+                                          _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                          _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                          _c_int, _c_int, _c_float, _c_int, _c_void_p, _c_size_t,
+                                          _c_void_p, _c_void_p]),
     "gemma_kv_append_bucket": (_c_int, [_PVOID, _PVOID, _PI32, _c_int, _c_int, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
                                         _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_void_p]),
@@ -158,6 +163,32 @@ def gemma_kv_append(k_cache: Sequence[Optional[torch.Tensor]],
         _dev_ptr(k_new), _dev_ptr(v_new), _dev_ptr(write_pos), B, n_new, n_kv, d, cap,
         int(bool(k_eq_v)), _dtype(k_new), _dev_ptr(device_error), _stream(stream))
     _check("gemma_kv_append", st)
+
+
+def gemma_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_cache, v_cache, owner_map,
+                             layer: int, k_new: Optional[torch.Tensor],
+                             v_new: Optional[torch.Tensor], write_pos: torch.Tensor,
+                             seq_lens: torch.Tensor, max_seq_len: int, *, kind: int, window: int,
+                             n_kv: int, k_eq_v: bool, scale: float,
+                             kv_capacity: Optional[int] = None,
+                             workspace: Optional[torch.Tensor] = None,
+                             device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Append this step's K/V row ([B][1][n_kv][d]) and decode, in one launch (bf16)."""
+    B = q.shape[0]
+    n_q, d = q.shape[-2], q.shape[-1]
+    n_layers = len(owner_map)
+    kc = _cache_of(k_cache, owner_map, layer)
+    cap = kv_capacity if kv_capacity is not None else kc.shape[2]
+    vcs = list(v_cache) if v_cache is not None else [None] * n_layers
+    ws_ptr = _dev_ptr(workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = library().gemma_attn_decode_append(
+        _dev_ptr(out), _dev_ptr(q), _ptr_array(list(k_cache)), _ptr_array(vcs),
+        _i32_array(owner_map), n_layers, layer, _dev_ptr(k_new), _dev_ptr(v_new),
+        _dev_ptr(write_pos), _dev_ptr(seq_lens), int(max_seq_len), B, int(kind), int(window), n_q,
+        int(n_kv), d, int(bool(k_eq_v)), int(cap), float(scale), _dtype(q), ws_ptr, ws_bytes,
+        _dev_ptr(device_error), _stream(stream))
+    _check("gemma_attn_decode_append", st)
 
 
 def gemma_kv_append_bucket(k_cache: Sequence[Optional[torch.Tensor]],

@@ -100,7 +100,8 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
               int max_seq_len, int n_tok, int batch, int kind, int window, int n_q, int n_kv,
               int head_dim, int k_eq_v, int kv_capacity, float scale, float softcap, int dtype,
               void* workspace, size_t workspace_bytes, uint32_t* device_error, void* stream,
-              const int32_t* n_real = nullptr) {
+              const int32_t* n_real = nullptr, const void* k_new = nullptr,
+              const void* v_new = nullptr, const int32_t* write_pos = nullptr) {
     if (batch < 0 || n_tok < 1) return GEMMA_ERR_INVALID_ARG;
     if (!std::isfinite(softcap) || softcap < 0.f) return GEMMA_ERR_INVALID_ARG;
     int st = check_shape(kind, window, n_q, n_kv, head_dim, dtype);
@@ -138,6 +139,9 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     p.v = vc;
     p.seq_lens = seq_lens;
     p.n_real = n_real;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.write_pos = write_pos;
     p.out = out;
     p.o_part = pl.ws_bytes ? static_cast<float*>(workspace) : nullptr;
     p.ml_part = pl.ws_bytes
@@ -302,6 +306,42 @@ int gemma_attn_softcap(void* out, const void* q, const void* const* k_cache,
     return attention(out, q, k_cache, v_cache, owner_map, n_layers, layer, seq_lens, max_seq_len,
                      n_new, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
                      softcap, dtype, workspace, workspace_bytes, device_error, stream);
+}
+
+int gemma_attn_decode_append(void* out, const void* q, void* const* k_cache, void* const* v_cache,
+                             const int32_t* owner_map, int n_layers, int layer, const void* k_new,
+                             const void* v_new, const int32_t* write_pos,
+                             const int32_t* seq_lens, int max_seq_len, int batch,
+                             gemma_layer_kind kind, int window, int n_q, int n_kv, int head_dim,
+                             int k_eq_v, int kv_capacity, float scale, gemma_dtype dtype,
+                             void* workspace, size_t workspace_bytes, uint32_t* device_error,
+                             void* stream) {
+    int o = 0;
+    int st = resolve_owner(owner_map, n_layers, layer, &o);
+    if (st != GEMMA_OK) return st;
+    const void* const* kcc = const_cast<const void* const*>(k_cache);
+    const void* const* vcc = const_cast<const void* const*>(v_cache);
+    if (o != layer)  // a shared layer appends nothing: plain decode against the owner's cache
+        return attention(out, q, kcc, vcc, owner_map, n_layers, layer, seq_lens, max_seq_len, 1,
+                         batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
+                         0.f, dtype, workspace, workspace_bytes, device_error, stream);
+    if (batch > 0 && (!k_new || !write_pos || (!k_eq_v && !v_new))) return GEMMA_ERR_INVALID_ARG;
+    if (batch > 0 && (!aligned16(k_new) || (!k_eq_v && !aligned16(v_new))))
+        return GEMMA_ERR_INVALID_ARG;
+    if (dtype != GEMMA_BF16) {
+        // the fp32 debug path keeps two launches: append, then attend
+        st = append_rows(k_cache, v_cache, owner_map, n_layers, layer, k_new, v_new, write_pos,
+                         nullptr, batch, 1, n_kv, head_dim, kv_capacity, k_eq_v, dtype,
+                         device_error, stream);
+        if (st != GEMMA_OK) return st;
+        return attention(out, q, kcc, vcc, owner_map, n_layers, layer, seq_lens, max_seq_len, 1,
+                         batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,
+                         0.f, dtype, workspace, workspace_bytes, device_error, stream);
+    }
+    return attention(out, q, kcc, vcc, owner_map, n_layers, layer, seq_lens, max_seq_len, 1, batch,
+                     kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale, 0.f, dtype,
+                     workspace, workspace_bytes, device_error, stream, nullptr, k_new,
+                     k_eq_v ? nullptr : v_new, write_pos);
 }
 
 int gemma_attn_prefill_bucket(void* out, const void* q, const void* const* k_cache,

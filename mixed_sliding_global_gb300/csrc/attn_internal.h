@@ -17,6 +17,11 @@ struct RowsParams {
     const void* v;            // owner layer's V cache (== k when k_eq_v)
     const int32_t* seq_lens;  // [B], tokens in the cache after this step's append
     const int32_t* n_real;    // [B] real tokens of a padded prefill bucket, or nullptr (all real)
+    // fused append (decode): this step's K/V rows [B][1][n_kv][D] written into the cache at
+    // write_pos[b] by the CTA that reads that slot; k_new == nullptr: no append
+    const void* k_new;
+    const void* v_new;
+    const int32_t* write_pos;
     void* out;                // [B][n_tok][n_q][D], written when n_split == 1
     float* o_part;            // [B][n_q][n_split][D]  unnormalised partial outputs
     float* ml_part;           // [B][n_q][n_split][2]  (running max in log2 units, sum)

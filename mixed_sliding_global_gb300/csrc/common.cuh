@@ -37,6 +37,12 @@ GEMMA_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
                  : "memory");
 }
 
+// Orders this thread's earlier generic-proxy global writes before later async-proxy (TMA)
+// reads of the same memory.
+GEMMA_DEVINL void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 GEMMA_DEVINL void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

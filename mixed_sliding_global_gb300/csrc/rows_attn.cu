@@ -175,6 +175,35 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
 
     if (warp == kConsumerWarps) {
         // ---------------- producer warp: tiled TMA loads of the K/V rows in range --------------
+        if (p.k_new) {
+            // fused append: the CTA whose chunk holds the new slot (split 0 when no chunk does)
+            // writes this KV head's new K/V row before any TMA load reads the cache
+            const int wp = __ldg(p.write_pos + b);
+            const bool in_range = wp >= first.lo && wp <= last.pos;
+            const bool writer = rt == 0 && (in_range ? (wp >= kb && wp < ke) : split == 0);
+            if (writer) {
+                if (wp < 0 || wp >= p.cap) {
+                    if (lane == 0) report(p.err, GEMMA_DEVERR_WRITE_POS);
+                } else {
+                    const size_t src = ((size_t)b * p.n_kv + kvh) * (size_t)D;
+                    const size_t dst = (((size_t)b * p.n_kv + kvh) * (size_t)p.cap + wp) * (size_t)D;
+                    for (int c = lane; c < D / 8; c += 32) {
+                        const uint4 kv4 = __ldg(reinterpret_cast<const uint4*>(
+                            reinterpret_cast<const __nv_bfloat16*>(p.k_new) + src) + c);
+                        reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(
+                            reinterpret_cast<const __nv_bfloat16*>(p.k) + dst))[c] = kv4;
+                        if (!p.k_eq_v) {
+                            const uint4 vv4 = __ldg(reinterpret_cast<const uint4*>(
+                                reinterpret_cast<const __nv_bfloat16*>(p.v_new) + src) + c);
+                            reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(
+                                reinterpret_cast<const __nv_bfloat16*>(p.v) + dst))[c] = vv4;
+                        }
+                    }
+                    fence_proxy_async_global();
+                }
+            }
+            __syncwarp();
+        }
         if (lane == 0) {
             const int row3 = b * p.n_kv + kvh;
             for (int t = 0; t < n_tiles; ++t) {
