@@ -154,10 +154,12 @@ class ClockSampler:
 # device state of a workload (seeded values drawn on the device)
 # ---------------------------------------------------------------------------------------------
 class DeviceState:
-    def __init__(self, w, seed, device, phys_of_layer=None, softcap=None, n_real=None):
+    def __init__(self, w, seed, device, phys_of_layer=None, softcap=None, n_real=None,
+                 fused=False):
         import mixed_sliding_global_gb300 as g
         self.g, self.w, self.device = g, w, device
         self.softcap = softcap
+        self.fused = fused  # decode: append inside the attention launch (one launch per layer)
         # padded prefill bucket: real rows per sequence (the rest pad the bucket to n_new)
         self.n_real = None if n_real is None else torch.tensor(n_real, dtype=torch.int32,
                                                                 device=device)
@@ -235,8 +237,25 @@ class DeviceState:
                                self.v_new[l], self.write_pos, k_eq_v=s.k_eq_v,
                                device_error=self.err)
 
+    def fused_call(self, l):
+        w, s = self.w, self.w.layers[l]
+        o = w.owner_map[l]
+        self.g.gemma_attn_decode_append(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l,
+                                        self.k_new[o], self.v_new[o], self.write_pos,
+                                        self.seq_lens, self.max_seq_len, kind=s.kind,
+                                        window=s.window, n_kv=s.n_kv, k_eq_v=s.k_eq_v,
+                                        scale=w.scale(l), workspace=self.ws,
+                                        device_error=self.err)
+
     def step(self, events=None):
         for l in range(self.w.n_layers):
+            if self.fused:
+                if events is not None:
+                    events[l][0].record()
+                self.fused_call(l)
+                if events is not None:
+                    events[l][1].record()
+                continue
             if self.w.is_owner(l):
                 self.append_call(l)
             if events is not None:
@@ -249,7 +268,7 @@ class DeviceState:
         n = 0
         w = self.w
         for l, s in enumerate(w.layers):
-            n += 1 if w.is_owner(l) else 0
+            n += 1 if w.is_owner(l) and not self.fused else 0
             n += 1
             if w.n_new == 1 and self.g.gemma_attn_workspace_size(
                     w.batch, s.kind, s.window, s.n_q, s.n_kv, s.head_dim, self.max_seq_len, 1) > 0:
@@ -344,11 +363,11 @@ def workload(name, batch=None, layers=None, offset=0):
 
 
 def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rotations=1,
-                    softcap=None, n_real=None):
+                    softcap=None, n_real=None, fused=False):
     """Capture one graph per step (rotating over `rotations` independent input copies) and
     time `steps` replays after `warmup` replays. Returns step time and, with per_launch, the
     mean duration of each layer's attention launch over the timed replays."""
-    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap, n_real)
+    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap, n_real, fused)
               for r in range(rotations)]
     for st in states:   # eager pass: sets kernel attributes, checks the error word
         st.step()
@@ -394,10 +413,10 @@ def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rot
     return ms, launch_ms, clk, info
 
 
-def e2e_run(w, phys, steps, warmup, device):
+def e2e_run(w, phys, steps, warmup, device, fused=False):
     """Same step through the public API, eager, with this step's inputs copied from pinned host
     memory and the outputs read back every step (the caches stay resident: they are state)."""
-    st = DeviceState(w, 4321, device, phys)
+    st = DeviceState(w, 4321, device, phys, fused=fused)
     host_in = {}
     for l in range(w.n_layers):
         for name in ("q", "k_new", "v_new"):
@@ -505,8 +524,10 @@ def run_native(args):
     unit = "GB/s" if decode else "TFLOP/s"
     scale = 1e9 if decode else 1e12
     work = step_work(w)
+    fused_main = w.n_new == 1 and not args.two_launch and args.softcap is None
     ms, launch_ms, clk, info = timed_graph_run(w, phys, args.steps, args.warmup, device, world,
-                                               per_launch=True, softcap=args.softcap)
+                                               per_launch=True, softcap=args.softcap,
+                                               fused=fused_main)
     ms = max_over_ranks(ms, world)
     value = job_value(work, world, ms, scale)
 
@@ -563,13 +584,15 @@ def run_native(args):
                        "l2": "inputs larger than L2 (each layer-step reads > 129 MB)"
                        if args.workload == "ragged_decode" else "inputs larger than L2",
                        "phys_caches": len(set(phys)) if phys else w.n_layers,
-                       **({"softcap": args.softcap} if args.softcap is not None else {})},
+                       **({"softcap": args.softcap} if args.softcap is not None else {}),
+                       "append": "inside the attention launch" if fused_main else
+                                 "separate launch"},
             "roofline": roof,
             "gpu_launches": info["launches_per_step"] * args.steps,
             "clocks": clk}
 
     if not args.quick:
-        e2e_ms, bi, bo = e2e_run(w, phys, max(3, args.steps // 4), 2, device)
+        e2e_ms, bi, bo = e2e_run(w, phys, max(3, args.steps // 4), 2, device, fused_main)
         e2e_ms = max_over_ranks(e2e_ms, world)
         line["e2e"] = {"value": world * work / (e2e_ms * 1e-3) / scale, "unit": unit,
                        "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
@@ -583,15 +606,21 @@ def run_native(args):
         # example value: the pages name an attention soft-cap without its value)
         # prefill_bucket: the prefill bucket padded, real lengths 512/384/256/128 of 512 (the
         # TFLOP/s count the real rows' work only)
+        # *_two_launch: the batch-1 decodes with a separate append launch per owner layer (the
+        # plain rows append inside the attention launch)
         for name in [n for n in ("prefill", "prefill_softcap", "prefill_bucket", "12b_decode",
-                                 "e4b_decode") if n != args.workload]:
+                                 "12b_decode_two_launch", "e4b_decode", "e4b_decode_two_launch")
+                     if n != args.workload]:
             cap2 = SOFTCAP_EXAMPLE if name == "prefill_softcap" else None
             real2 = BUCKET_REAL_EXAMPLE if name == "prefill_bucket" else None
-            w2, phys2 = workload("prefill" if name.startswith("prefill") else name)
-            rot = 12 if name == "e4b_decode" else 1   # e4b inputs (32 MB) rotate past L2
+            fused2 = not name.startswith("prefill") and not name.endswith("_two_launch")
+            w2, phys2 = workload("prefill" if name.startswith("prefill") else
+                                 name.replace("_two_launch", ""))
+            rot = 12 if name.startswith("e4b_decode") else 1   # e4b inputs rotate past L2
             ms2, lm2, clk2, info2 = timed_graph_run(w2, phys2, args.steps, args.warmup, device,
                                                     world, per_launch=(w2.n_new > 1),
-                                                    rotations=rot, softcap=cap2, n_real=real2)
+                                                    rotations=rot, softcap=cap2, n_real=real2,
+                                                    fused=fused2)
             ms2 = max_over_ranks(ms2, world)
             d2 = w2.n_new == 1
             u2, sc2 = ("GB/s", 1e9) if d2 else ("TFLOP/s", 1e12)
@@ -643,6 +672,9 @@ def main():
                     help="fewer ragged layer-steps (profiling captures only; not a bench line)")
     ap.add_argument("--layer-offset", type=int, default=0,
                     help="first ragged layer (profiling captures only; not a bench line)")
+    ap.add_argument("--two-launch", action="store_true",
+                    help="decode workloads: a separate append launch before each attention "
+                         "launch (default: the append inside the attention launch)")
     ap.add_argument("--softcap", type=float, default=None,
                     help="time the workload through the soft-capped entry point with this cap")
     ap.add_argument("--quick", action="store_true",
