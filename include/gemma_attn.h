@@ -50,7 +50,13 @@
 extern "C" {
 #endif
 
-typedef enum { GEMMA_SLIDING = 0, GEMMA_GLOBAL = 1 } gemma_layer_kind;
+/* GEMMA_SLIDING_RING: a sliding layer whose cache is a ring of kv_capacity slots holding the
+ * most recent tokens, position p at slot p % kv_capacity (the pages' fixed KV_MAX buffer sized
+ * to the window rather than the context). kv_capacity must be a multiple of 128 and at least
+ * window + n_new - 1 (every key a step attends is still in the ring), else
+ * GEMMA_ERR_UNSUPPORTED / GEMMA_ERR_CAPACITY; seq_lens and max_seq_len may exceed it. Its rows
+ * are written with gemma_kv_append_ring (or gemma_attn_decode_append, which wraps the same way). */
+typedef enum { GEMMA_SLIDING = 0, GEMMA_GLOBAL = 1, GEMMA_SLIDING_RING = 2 } gemma_layer_kind;
 typedef enum { GEMMA_BF16 = 0, GEMMA_FP32 = 1 } gemma_dtype;
 typedef enum {
     GEMMA_OK = 0,
@@ -88,6 +94,17 @@ int gemma_kv_append(void* const* k_cache, void* const* v_cache, const int32_t* o
                     const int32_t* write_pos, int batch, int n_new, int n_kv, int head_dim,
                     int kv_capacity, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
                     void* stream);
+
+/*
+ * gemma_kv_append_ring -- gemma_kv_append into a ring cache (GEMMA_SLIDING_RING): row t of
+ * sequence b goes to slot (write_pos[b] + t) % kv_capacity; write_pos[b] >= 0 may exceed the
+ * capacity; n_new <= kv_capacity.
+ */
+int gemma_kv_append_ring(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
+                         int n_layers, int layer, const void* k_new, const void* v_new,
+                         const int32_t* write_pos, int batch, int n_new, int n_kv, int head_dim,
+                         int kv_capacity, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
+                         void* stream);
 
 /*
  * gemma_attn_decode -- the decode bucket: one query token per sequence (n_tok = 1), whose

@@ -7,11 +7,12 @@ computation runs in the library's CUDA kernels; there is no CPU or PyTorch fallb
 loading fails loudly when the library has not been built.
 """
 from .binding import (  # noqa: F401
-    GEMMA_SLIDING, GEMMA_GLOBAL, GEMMA_BF16, GEMMA_FP32, GEMMA_OK,
+    GEMMA_SLIDING, GEMMA_GLOBAL, GEMMA_SLIDING_RING, GEMMA_BF16, GEMMA_FP32, GEMMA_OK,
     GEMMA_DEVERR_SEQ_LEN, GEMMA_DEVERR_WRITE_POS, GEMMA_DEVERR_TIMEOUT, GEMMA_DEVERR_N_REAL,
     GemmaError, library, library_path, exported_symbols,
     gemma_kv_append, gemma_attn_decode, gemma_attn_decode_static, gemma_attn_prefill, gemma_attn_softcap,
     gemma_kv_append_bucket, gemma_attn_prefill_bucket, gemma_attn_decode_append,
+    gemma_kv_append_ring,
     gemma_attn_workspace_size,
     gemma_status_string, gemma_abi_version,
 )

@@ -10,7 +10,7 @@ import torch
 
 from . import _build
 
-GEMMA_SLIDING, GEMMA_GLOBAL = 0, 1
+GEMMA_SLIDING, GEMMA_GLOBAL, GEMMA_SLIDING_RING = 0, 1, 2
 GEMMA_BF16, GEMMA_FP32 = 0, 1
 GEMMA_OK = 0
 GEMMA_DEVERR_SEQ_LEN, GEMMA_DEVERR_WRITE_POS, GEMMA_DEVERR_TIMEOUT = 1, 2, 4
@@ -45,6 +45,9 @@ _SIGNATURES = {
                                           _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           _c_int, _c_int, _c_float, _c_int, _c_void_p, _c_size_t,
                                           _c_void_p, _c_void_p]),
+    "gemma_kv_append_ring": (_c_int, [_PVOID, _PVOID, _PI32, _c_int, _c_int, _c_void_p,
+                                      _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _c_void_p, _c_void_p]),
     "gemma_kv_append_bucket": (_c_int, [_PVOID, _PVOID, _PI32, _c_int, _c_int, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
                                         _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_void_p]),
@@ -189,6 +192,25 @@ def gemma_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_cache, v_cach
         int(n_kv), d, int(bool(k_eq_v)), int(cap), float(scale), _dtype(q), ws_ptr, ws_bytes,
         _dev_ptr(device_error), _stream(stream))
     _check("gemma_attn_decode_append", st)
+
+
+def gemma_kv_append_ring(k_cache: Sequence[Optional[torch.Tensor]],
+                         v_cache: Optional[Sequence[Optional[torch.Tensor]]],
+                         owner_map: Sequence[int], layer: int, k_new: torch.Tensor,
+                         v_new: Optional[torch.Tensor], write_pos: torch.Tensor, *, k_eq_v: bool,
+                         kv_capacity: Optional[int] = None,
+                         device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """gemma_kv_append into a ring cache: row t goes to slot (write_pos[b] + t) % capacity."""
+    B, n_new, n_kv, d = k_new.shape
+    n_layers = len(owner_map)
+    kc = k_cache[int(owner_map[layer])]
+    cap = kv_capacity if kv_capacity is not None else (kc.shape[2] if kc is not None else 0)
+    vcs = list(v_cache) if v_cache is not None else [None] * n_layers
+    st = library().gemma_kv_append_ring(
+        _ptr_array(list(k_cache)), _ptr_array(vcs), _i32_array(owner_map), n_layers, layer,
+        _dev_ptr(k_new), _dev_ptr(v_new), _dev_ptr(write_pos), B, n_new, n_kv, d, cap,
+        int(bool(k_eq_v)), _dtype(k_new), _dev_ptr(device_error), _stream(stream))
+    _check("gemma_kv_append_ring", st)
 
 
 def gemma_kv_append_bucket(k_cache: Sequence[Optional[torch.Tensor]],

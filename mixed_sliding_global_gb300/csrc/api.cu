@@ -39,8 +39,9 @@ bool group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
 long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
 int check_shape(int kind, int window, int n_q, int n_kv, int head_dim, int dtype) {
-    if (kind != GEMMA_SLIDING && kind != GEMMA_GLOBAL) return GEMMA_ERR_INVALID_ARG;
-    if (kind == GEMMA_SLIDING && window < 1) return GEMMA_ERR_INVALID_ARG;
+    if (kind != GEMMA_SLIDING && kind != GEMMA_GLOBAL && kind != GEMMA_SLIDING_RING)
+        return GEMMA_ERR_INVALID_ARG;
+    if (kind != GEMMA_GLOBAL && window < 1) return GEMMA_ERR_INVALID_ARG;
     if (n_q < 1 || n_kv < 1 || n_q % n_kv != 0) return GEMMA_ERR_INVALID_ARG;
     if (dtype != GEMMA_BF16 && dtype != GEMMA_FP32) return GEMMA_ERR_INVALID_ARG;
     if (!head_dim_ok(head_dim) || !group_ok(n_q / n_kv)) return GEMMA_ERR_UNSUPPORTED;
@@ -73,7 +74,10 @@ Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim,
     Plan pl{1, 1 << 30, 0, 0};
     if (n_tok != 1) return pl;
     const long long T = gemma::kKeyTile;
-    const long long n_read = kind == GEMMA_SLIDING && window < max_seq_len ? window : max_seq_len;
+    long long n_read = kind != GEMMA_GLOBAL && window < max_seq_len ? window : max_seq_len;
+    // a ring cache's key tiles start at multiples of the tile (so that none wraps): up to T - 1
+    // keys before the window join the range
+    if (kind == GEMMA_SLIDING_RING) n_read += T - 1;
     const long long total = (long long)batch * n_kv * n_read;
     const long long one_per_sm = round_up((total + n_sm - 1) / n_sm, T);
     const long long eight_per_sm =
@@ -111,7 +115,13 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     if (st != GEMMA_OK) return st;
     if (kv_capacity < 1 || max_seq_len < n_tok || !std::isfinite(scale) || !(scale > 0.f))
         return GEMMA_ERR_INVALID_ARG;
-    if (max_seq_len > kv_capacity) return GEMMA_ERR_CAPACITY;
+    const bool ring = kind == GEMMA_SLIDING_RING;
+    if (ring) {
+        if (kv_capacity % 128 != 0) return GEMMA_ERR_UNSUPPORTED;
+        if ((long long)kv_capacity < (long long)window + n_tok - 1) return GEMMA_ERR_CAPACITY;
+    } else if (max_seq_len > kv_capacity) {
+        return GEMMA_ERR_CAPACITY;
+    }
     if (batch > 65535) return GEMMA_ERR_UNSUPPORTED;
     if (batch == 0) return GEMMA_OK;
     if (!out || !q || !seq_lens || !k_cache || !k_cache[o]) return GEMMA_ERR_INVALID_ARG;
@@ -154,7 +164,8 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     p.G = n_q / n_kv;
     p.cap = kv_capacity;
     p.window = window;
-    p.is_sliding = kind == GEMMA_SLIDING;
+    p.is_sliding = kind != GEMMA_GLOBAL;
+    p.ring = ring ? kv_capacity : 0;
     p.k_eq_v = k_eq_v ? 1 : 0;
     p.max_seq_len = max_seq_len;
     p.n_split = pl.n_split;
@@ -186,8 +197,8 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
 
 int append_rows(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
                 int n_layers, int layer, const void* k_new, const void* v_new,
-                const int32_t* write_pos, const int32_t* n_real, int batch, int n_new, int n_kv,
-                int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
+                const int32_t* write_pos, const int32_t* n_real, int ring, int batch, int n_new,
+                int n_kv, int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
                 uint32_t* device_error, void* stream);
 
 }  // namespace
@@ -214,8 +225,18 @@ int gemma_kv_append(void* const* k_cache, void* const* v_cache, const int32_t* o
                     int kv_capacity, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
                     void* stream) {
     return append_rows(k_cache, v_cache, owner_map, n_layers, layer, k_new, v_new, write_pos,
-                       nullptr, batch, n_new, n_kv, head_dim, kv_capacity, k_eq_v, dtype,
+                       nullptr, 0, batch, n_new, n_kv, head_dim, kv_capacity, k_eq_v, dtype,
                        device_error, stream);
+}
+
+int gemma_kv_append_ring(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
+                         int n_layers, int layer, const void* k_new, const void* v_new,
+                         const int32_t* write_pos, int batch, int n_new, int n_kv, int head_dim,
+                         int kv_capacity, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
+                         void* stream) {
+    return append_rows(k_cache, v_cache, owner_map, n_layers, layer, k_new, v_new, write_pos,
+                       nullptr, kv_capacity, batch, n_new, n_kv, head_dim, kv_capacity, k_eq_v,
+                       dtype, device_error, stream);
 }
 
 int gemma_kv_append_bucket(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
@@ -225,7 +246,7 @@ int gemma_kv_append_bucket(void* const* k_cache, void* const* v_cache, const int
                            uint32_t* device_error, void* stream) {
     if (!n_real && batch > 0 && n_new > 0) return GEMMA_ERR_INVALID_ARG;
     return append_rows(k_cache, v_cache, owner_map, n_layers, layer, k_new, v_new, write_pos,
-                       n_real, batch, n_new, n_kv, head_dim, kv_capacity, k_eq_v, dtype,
+                       n_real, 0, batch, n_new, n_kv, head_dim, kv_capacity, k_eq_v, dtype,
                        device_error, stream);
 }
 
@@ -235,8 +256,8 @@ namespace {
 
 int append_rows(void* const* k_cache, void* const* v_cache, const int32_t* owner_map,
                 int n_layers, int layer, const void* k_new, const void* v_new,
-                const int32_t* write_pos, const int32_t* n_real, int batch, int n_new, int n_kv,
-                int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
+                const int32_t* write_pos, const int32_t* n_real, int ring, int batch, int n_new,
+                int n_kv, int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
                 uint32_t* device_error, void* stream) {
     if (batch < 0 || n_new < 0 || n_kv < 1 || kv_capacity < 1) return GEMMA_ERR_INVALID_ARG;
     if (dtype != GEMMA_BF16 && dtype != GEMMA_FP32) return GEMMA_ERR_INVALID_ARG;
@@ -260,7 +281,8 @@ int append_rows(void* const* k_cache, void* const* v_cache, const int32_t* owner
     if (n_sm < 0) return GEMMA_ERR_CUDA;
     const int row_bytes = head_dim * (dtype == GEMMA_BF16 ? 2 : 4);
     cudaError_t e = gemma::launch_kv_append(k_cache[layer], vc, k_new, vc ? v_new : nullptr,
-                                            write_pos, n_real, batch, n_new, n_kv, kv_capacity,
+                                            write_pos, n_real, ring, batch, n_new, n_kv,
+                                            kv_capacity,
                                             row_bytes, device_error, n_sm,
                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GEMMA_OK : GEMMA_ERR_CUDA;
@@ -331,8 +353,8 @@ int gemma_attn_decode_append(void* out, const void* q, void* const* k_cache, voi
     if (dtype != GEMMA_BF16) {
         // the fp32 debug path keeps two launches: append, then attend
         st = append_rows(k_cache, v_cache, owner_map, n_layers, layer, k_new, v_new, write_pos,
-                         nullptr, batch, 1, n_kv, head_dim, kv_capacity, k_eq_v, dtype,
-                         device_error, stream);
+                         nullptr, kind == GEMMA_SLIDING_RING ? kv_capacity : 0, batch, 1, n_kv,
+                         head_dim, kv_capacity, k_eq_v, dtype, device_error, stream);
         if (st != GEMMA_OK) return st;
         return attention(out, q, kcc, vcc, owner_map, n_layers, layer, seq_lens, max_seq_len, 1,
                          batch, kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale,

@@ -28,6 +28,7 @@ struct RowsParams {
     uint32_t* err;            // optional device error word
     int n_tok, n_q, n_kv, G, cap, window, is_sliding, k_eq_v;
     int max_seq_len;
+    int ring;                 // ring cache of this many slots (position p at p % ring), or 0
     int n_split;              // key chunks per row tile (1: write `out` directly)
     int chunk;                // keys per chunk (multiple of the key tile)
     int n_stages;             // smem pipeline depth (bf16 kernel)
@@ -55,8 +56,8 @@ cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out
 bool prefill_tc_supported(int head_dim);
 cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cudaStream_t st);
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
-                             const int32_t* write_pos, const int32_t* n_real, int batch,
-                             int n_new, int n_kv,
+                             const int32_t* write_pos, const int32_t* n_real, int ring,
+                             int batch, int n_new, int n_kv,
                              int capacity, int row_bytes, uint32_t* err, int n_sm,
                              cudaStream_t st);
 

@@ -2,6 +2,7 @@
 //
 //   cache[b][h][write_pos[b] + t][:] = new[b][t][h][:]     for t < n_real[b] (all n_new rows
 //                                                           when n_real is null)
+// and, into a ring cache of R slots, at slot (write_pos[b] + t) % R.
 //
 // "Gemma-4-E4B-it on AWS Inferentia2" ("Decode neff") keeps the KV buffers on the device and
 // updates them in place each step; its one-hot masked write exists only to keep a traced
@@ -19,7 +20,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
                                                         const uint8_t* __restrict__ vn,
                                                         const int32_t* __restrict__ write_pos,
                                                         const int32_t* __restrict__ n_real,
-                                                        int batch, int n_new, int n_kv,
+                                                        int ring, int batch, int n_new, int n_kv,
                                                         int capacity, int row_bytes,
                                                         uint32_t* err) {
     const int chunks = row_bytes / 16;
@@ -39,11 +40,12 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
             continue;
         }
         if (t >= nr) continue;  // a pad row of a padded bucket
-        if (pos < 0 || (long long)pos + nr > capacity) {
+        if (pos < 0 || (!ring && (long long)pos + nr > capacity)) {
             if (t == 0 && h == 0 && ch == 0) report(err, GEMMA_DEVERR_WRITE_POS);
             continue;
         }
-        const size_t dst = (((size_t)b * n_kv + h) * (size_t)capacity + (size_t)(pos + t)) *
+        const long long slot = ring ? ((long long)pos + t) % ring : (long long)pos + t;
+        const size_t dst = (((size_t)b * n_kv + h) * (size_t)capacity + (size_t)slot) *
                                (size_t)row_bytes + (size_t)ch * 16;
         const size_t src = (size_t)row * row_bytes + (size_t)ch * 16;
         *reinterpret_cast<uint4*>(kc + dst) = __ldg(reinterpret_cast<const uint4*>(kn + src));
@@ -52,9 +54,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
 }
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
-                             const int32_t* write_pos, const int32_t* n_real, int batch,
-                             int n_new, int n_kv, int capacity, int row_bytes, uint32_t* err,
-                             int n_sm, cudaStream_t st) {
+                             const int32_t* write_pos, const int32_t* n_real, int ring,
+                             int batch, int n_new, int n_kv, int capacity, int row_bytes,
+                             uint32_t* err, int n_sm, cudaStream_t st) {
     const long long total = (long long)batch * n_new * n_kv * (row_bytes / 16);
     long long blocks = (total + 255) / 256;
     const long long cap_blocks = (long long)n_sm * 8;
@@ -63,7 +65,7 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, co
     kv_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(
         static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
         static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), write_pos, n_real,
-        batch, n_new, n_kv, capacity, row_bytes, err);
+        ring, batch, n_new, n_kv, capacity, row_bytes, err);
     return cudaGetLastError();
 }
 

@@ -165,13 +165,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the i-th real token sits at len - n_real + i, the pad rows' outputs are zero
     const int n_real = p.n_real ? __ldg(p.n_real + b) : p.n_tok;
     const bool bad_real = n_real < 0 || n_real > p.n_tok;
-    const bool bad = bad_real || len < n_real || len > p.cap || len > p.max_seq_len;
+    const bool bad = bad_real || len < n_real || (!p.ring && len > p.cap) || len > p.max_seq_len;
     const int n_rows_real = bad ? 0 : max(0, min(128, n_real * p.G - row0));  // rows that attend
 
     // key range of the tile: from the first row's window start to the last real row's position
     const int tok_first = row0 / p.G, tok_last = (row0 + max(n_rows_real, 1) - 1) / p.G;
     const int pos_first = len - n_real + tok_first, pos_last = len - n_real + tok_last;
-    const int k_begin = p.is_sliding ? max(0, pos_first - p.window + 1) : 0;
+    // (a ring cache's tiles start at multiples of the tile, so that none wraps around the ring;
+    // the rows' masks drop the keys before the window)
+    const int k_begin = p.is_sliding ? (max(0, pos_first - p.window + 1) & (p.ring ? ~(kTcKeys - 1) : ~0))
+                                     : 0;
     const int k_end = pos_last + 1;
     const int n_tiles = n_rows_real == 0 ? 0 : (k_end - k_begin + kTcKeys - 1) / kTcKeys;
     // K/V ring split: with K = V one ring of NS slots; otherwise NV slots for V (V is needed
@@ -213,9 +216,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             auto load = [&](const CUtensorMap* map, int slot, int t) {
                 uint8_t* dst = slots + slot * Lay::SLOT;
                 mbar_arrive_expect_tx(&kv_full[slot], Lay::SLOT);
+                const int key0 = k_begin + t * kTcKeys;
+                const int slot0 = p.ring ? key0 % p.ring : key0;  // cache slot of the first key
                 for (int c = 0; c < Lay::CHUNKS; ++c)
-                    tma_load_3d(dst + c * kTcKeys * 128, map, (int)h * DH + c * 64,
-                                k_begin + t * kTcKeys, row3, &kv_full[slot]);
+                    tma_load_3d(dst + c * kTcKeys * 128, map, (int)h * DH + c * 64, slot0, row3,
+                                &kv_full[slot]);
             };
             bool ok = true;
             // ring cursors (slot, phase of the current pass, whether a pass has completed):

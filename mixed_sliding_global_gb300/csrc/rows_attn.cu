@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     const bool direct = p.n_split == 1;
     const int len = __ldg(p.seq_lens + b);
 
-    if (len < p.n_tok || len > p.cap || len > p.max_seq_len) {
+    if (len < p.n_tok || (!p.ring && len > p.cap) || len > p.max_seq_len) {
         if (split == 0) {
             if (threadIdx.x == 0) report(p.err, GEMMA_DEVERR_SEQ_LEN);
             if (direct) zero_rows<__nv_bfloat16>(p, b, kvh, row0, n_rows, D);
@@ -126,7 +126,10 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     // keys any row of this tile may attend, then this CTA's chunk of them
     const RowInfo first = row_info(p, len, kvh, row0);
     const RowInfo last = row_info(p, len, kvh, row0 + n_rows - 1);
-    const int kb = first.lo + split * p.chunk;
+    // a ring cache's chunks start at multiples of the key tile, so that no tile wraps around the
+    // ring (the rows' masks drop the keys before the window)
+    const int base = p.ring ? (first.lo & ~(T - 1)) : first.lo;
+    const int kb = base + split * p.chunk;
     const int ke = min(last.pos + 1, kb + p.chunk);
     if (kb >= ke) return;  // empty chunk: the combine pass skips it
     const int n_keys = ke - kb;
@@ -182,11 +185,13 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
             const bool in_range = wp >= first.lo && wp <= last.pos;
             const bool writer = rt == 0 && (in_range ? (wp >= kb && wp < ke) : split == 0);
             if (writer) {
-                if (wp < 0 || wp >= p.cap) {
+                if (wp < 0 || (!p.ring && wp >= p.cap)) {
                     if (lane == 0) report(p.err, GEMMA_DEVERR_WRITE_POS);
                 } else {
                     const size_t src = ((size_t)b * p.n_kv + kvh) * (size_t)D;
-                    const size_t dst = (((size_t)b * p.n_kv + kvh) * (size_t)p.cap + wp) * (size_t)D;
+                    const int slot = p.ring ? wp % p.ring : wp;
+                    const size_t dst =
+                        (((size_t)b * p.n_kv + kvh) * (size_t)p.cap + slot) * (size_t)D;
                     for (int c = lane; c < D / 8; c += 32) {
                         const uint4 kv4 = __ldg(reinterpret_cast<const uint4*>(
                             reinterpret_cast<const __nv_bfloat16*>(p.k_new) + src) + c);
@@ -211,11 +216,13 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
                 if (t >= S && !mbar_wait(&empty[s], ((t / S) - 1) & 1, p.err)) break;
                 uint8_t* dk = ring + s * stage_bytes;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+                const int key0 = kb + t * T;
+                const int slot0 = p.ring ? key0 % p.ring : key0;  // cache slot of the tile's first key
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
-                    tma_load_3d(dk + c * Lay::BOX, &kmap, c * 64, kb + t * T, row3, &full[s]);
+                    tma_load_3d(dk + c * Lay::BOX, &kmap, c * 64, slot0, row3, &full[s]);
                     if (nops == 2)
-                        tma_load_3d(dk + Lay::TILE + c * Lay::BOX, &vmap, c * 64, kb + t * T, row3,
+                        tma_load_3d(dk + Lay::TILE + c * Lay::BOX, &vmap, c * 64, slot0, row3,
                                     &full[s]);
                 }
             }
@@ -434,7 +441,7 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
     // real tokens of this sequence (a padded bucket's first n_real rows; all rows otherwise)
     const int n_real = p.n_real ? __ldg(p.n_real + b) : p.n_tok;
     const bool bad_real = n_real < 0 || n_real > p.n_tok;
-    const bool bad = bad_real || len < n_real || len > p.cap || len > p.max_seq_len;
+    const bool bad = bad_real || len < n_real || (!p.ring && len > p.cap) || len > p.max_seq_len;
     if (bad || token >= n_real) {  // a bad sequence, or a pad row: zero output
         if (split == 0) {
             if (bad && lane == 0) report(p.err, bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
@@ -445,7 +452,8 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
     }
     const int pos = len - n_real + token;
     const int lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
-    const int kb = lo + split * p.chunk;
+    // chunks as in the bf16 kernel (a ring cache's start at multiples of the key tile)
+    const int kb = (p.ring ? (lo & ~(kKeyTile - 1)) : lo) + split * p.chunk;
     const int ke = min(pos + 1, kb + p.chunk);
     if (kb >= ke) return;
 
@@ -461,10 +469,11 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
         acc[e] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
-    for (int j = kb; j < ke; ++j) {
+    for (int j = max(kb, lo); j < ke; ++j) {
+        const size_t row = (size_t)(p.ring ? j % p.ring : j);  // cache slot of key j
         float dot = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) dot = fmaf(qr[e], K[(size_t)j * D + lane + 32 * e], dot);
+        for (int e = 0; e < E; ++e) dot = fmaf(qr[e], K[row * D + lane + 32 * e], dot);
         float s = warp_sum(dot) * p.scale;
         if (p.softcap > 0.f) s = p.softcap * tanhf(s / p.softcap);
         const float m_new = fmaxf(m, s);
@@ -472,7 +481,7 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
         const float w = expf(s - m_new);
         l = l * alpha + w;
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, V[(size_t)j * D + lane + 32 * e], acc[e] * alpha);
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, V[row * D + lane + 32 * e], acc[e] * alpha);
         m = m_new;
     }
     if (direct) {
@@ -510,11 +519,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const RowsPara
     const int len = __ldg(p.seq_lens + b);
     OutT* dst = reinterpret_cast<OutT*>(p.out) + ((size_t)b * p.n_q + head) * (size_t)D;
     const int tid = threadIdx.x;
-    if (len < 1 || len > p.cap || len > p.max_seq_len) {
+    if (len < 1 || (!p.ring && len > p.cap) || len > p.max_seq_len) {
         for (int c = tid; c < D; c += blockDim.x) dst[c] = OutT(0.f);
         return;
     }
-    const int lo = p.is_sliding ? max(0, len - p.window) : 0;
+    int lo = p.is_sliding ? max(0, len - p.window) : 0;
+    if (p.ring) lo &= ~(kKeyTile - 1);  // chunks of a ring cache start at a tile boundary
     const int nc = min(p.n_split, (len - lo + p.chunk - 1) / p.chunk);
     const size_t base = ((size_t)b * p.n_q + head) * p.n_split;
     if (tid < 32) {

@@ -102,6 +102,21 @@ def test_bucket_entry_points_need_n_real():
                                            None, 0, None, None) == 0   # empty batch
 
 
+@pytest.mark.parametrize("cap,window,status", [(1000, 512, UNSUPPORTED),   # not a multiple of 128
+                                                (512, 640, CAPACITY)])        # smaller than the window
+def test_ring_capacity_checks(cap, window, status):
+    """A ring cache (kind 2) needs a capacity that is a multiple of 128 and holds the window."""
+    assert decode(kind=2, window=window, cap=cap, max_seq_len=4096, k_eq_v=0,
+                  vc=(FAKE,)) == status
+
+
+def test_ring_prefill_needs_window_plus_new_tokens():
+    st = lib().gemma_attn_prefill(FAKE, FAKE, _ptrs(FAKE), _ptrs(FAKE), _i32(0), 1, 0, FAKE, 4096,
+                                  130, 1, 2, 1024, 4, 1, 64, 0, 1152, 0.125, 0, None, 0, None,
+                                  None)
+    assert st == CAPACITY   # 1152 < 1024 + 130 - 1
+
+
 def test_empty_batch_is_ok_without_touching_the_device():
     assert decode(batch=0) == 0
     assert lib().gemma_attn_prefill(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, 64,
