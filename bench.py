@@ -40,6 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 RAGGED_PHYS_LAYERS = 6   # distinct caches for 48 ragged layer-steps (one 5:1 period)
 SOFTCAP_EXAMPLE = 50.0   # attention-logit soft-cap used to time the soft-capped entry point
 BUCKET_REAL_EXAMPLE = [512, 384, 256, 128]   # real rows per sequence of the padded bucket timed
+RING_EXAMPLE = 1024      # ring slots of the sliding layers' caches (the 12B window)
 
 # dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
 # captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
@@ -155,11 +156,12 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------------
 class DeviceState:
     def __init__(self, w, seed, device, phys_of_layer=None, softcap=None, n_real=None,
-                 fused=False):
+                 fused=False, ring=None):
         import mixed_sliding_global_gb300 as g
         self.g, self.w, self.device = g, w, device
         self.softcap = softcap
         self.fused = fused  # decode: append inside the attention launch (one launch per layer)
+        self.ring = ring    # sliding layers' caches: rings of this many slots (None: linear)
         # padded prefill bucket: real rows per sequence (the rest pad the bucket to n_new)
         self.n_real = None if n_real is None else torch.tensor(n_real, dtype=torch.int32,
                                                                 device=device)
@@ -180,8 +182,13 @@ class DeviceState:
             if w.is_owner(l):
                 p = phys[l]
                 if p not in kc_phys:
-                    kc_phys[p] = self._cache(s, B, cap, dt)
-                    vc_phys[p] = None if s.k_eq_v else self._cache(s, B, cap, dt)
+                    if ring and s.kind == synth.SLIDING:
+                        # a ring holds the last `ring` tokens: every slot is a real past token
+                        kc_phys[p] = self._randn((B, s.n_kv, ring, s.head_dim), dt)
+                        vc_phys[p] = None if s.k_eq_v else self._randn((B, s.n_kv, ring, s.head_dim), dt)
+                    else:
+                        kc_phys[p] = self._cache(s, B, cap, dt)
+                        vc_phys[p] = None if s.k_eq_v else self._cache(s, B, cap, dt)
                 self.kc[l], self.vc[l] = kc_phys[p], vc_phys[p]
                 self.k_new[l] = self._randn((B, w.n_new, s.n_kv, s.head_dim), dt)
                 if not s.k_eq_v:
@@ -189,8 +196,8 @@ class DeviceState:
             self.q[l] = self._randn((B, w.n_new, s.n_q, s.head_dim), dt)
             self.out[l] = torch.empty_like(self.q[l])
         msl = max(w.ctx_lens)
-        ws = max(g.gemma_attn_workspace_size(B, s.kind, s.window, s.n_q, s.n_kv, s.head_dim, msl,
-                                             w.n_new) for s in w.layers)
+        ws = max(g.gemma_attn_workspace_size(B, self.kind_of(s), s.window, s.n_q, s.n_kv,
+                                             s.head_dim, msl, w.n_new) for s in w.layers)
         self.ws = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
         self.max_seq_len = msl
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -209,9 +216,12 @@ class DeviceState:
             c[b, :, lo:ctx].copy_(self._randn((s.n_kv, ctx - lo, s.head_dim), dt))
         return c
 
+    def kind_of(self, s):
+        return self.g.GEMMA_SLIDING_RING if self.ring and s.kind == synth.SLIDING else s.kind
+
     def layer_call(self, l):
         w, s = self.w, self.w.layers[l]
-        kw = dict(kind=s.kind, window=s.window, n_kv=s.n_kv, k_eq_v=s.k_eq_v, scale=w.scale(l),
+        kw = dict(kind=self.kind_of(s), window=s.window, n_kv=s.n_kv, k_eq_v=s.k_eq_v, scale=w.scale(l),
                   workspace=self.ws, device_error=self.err)
         if self.softcap is not None:
             self.g.gemma_attn_softcap(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l,
@@ -228,6 +238,11 @@ class DeviceState:
 
     def append_call(self, l):
         s = self.w.layers[l]
+        if self.ring and s.kind == synth.SLIDING:
+            self.g.gemma_kv_append_ring(self.kc, self.vc, self.w.owner_map, l, self.k_new[l],
+                                        self.v_new[l], self.write_pos, k_eq_v=s.k_eq_v,
+                                        device_error=self.err)
+            return
         if self.n_real is not None:
             self.g.gemma_kv_append_bucket(self.kc, self.vc, self.w.owner_map, l, self.k_new[l],
                                           self.v_new[l], self.write_pos, self.n_real,
@@ -242,7 +257,7 @@ class DeviceState:
         o = w.owner_map[l]
         self.g.gemma_attn_decode_append(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l,
                                         self.k_new[o], self.v_new[o], self.write_pos,
-                                        self.seq_lens, self.max_seq_len, kind=s.kind,
+                                        self.seq_lens, self.max_seq_len, kind=self.kind_of(s),
                                         window=s.window, n_kv=s.n_kv, k_eq_v=s.k_eq_v,
                                         scale=w.scale(l), workspace=self.ws,
                                         device_error=self.err)
@@ -363,11 +378,11 @@ def workload(name, batch=None, layers=None, offset=0):
 
 
 def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rotations=1,
-                    softcap=None, n_real=None, fused=False):
+                    softcap=None, n_real=None, fused=False, ring=None):
     """Capture one graph per step (rotating over `rotations` independent input copies) and
     time `steps` replays after `warmup` replays. Returns step time and, with per_launch, the
     mean duration of each layer's attention launch over the timed replays."""
-    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap, n_real, fused)
+    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap, n_real, fused, ring)
               for r in range(rotations)]
     for st in states:   # eager pass: sets kernel attributes, checks the error word
         st.step()
@@ -586,7 +601,8 @@ def run_native(args):
                        "phys_caches": len(set(phys)) if phys else w.n_layers,
                        **({"softcap": args.softcap} if args.softcap is not None else {}),
                        "append": "inside the attention launch" if fused_main else
-                                 "separate launch"},
+                                 "separate launch",
+                       "cache_gb": info["cache_bytes"] / 1e9},
             "roofline": roof,
             "gpu_launches": info["launches_per_step"] * args.steps,
             "clocks": clk}
@@ -608,19 +624,22 @@ def run_native(args):
         # TFLOP/s count the real rows' work only)
         # *_two_launch: the batch-1 decodes with a separate append launch per owner layer (the
         # plain rows append inside the attention launch)
+        # ragged_decode_ring: the headline workload with its sliding layers' caches as rings of
+        # 1024 slots (the window) instead of 16448 rows
         for name in [n for n in ("prefill", "prefill_softcap", "prefill_bucket", "12b_decode",
-                                 "12b_decode_two_launch", "e4b_decode", "e4b_decode_two_launch")
-                     if n != args.workload]:
+                                 "12b_decode_two_launch", "e4b_decode", "e4b_decode_two_launch",
+                                 "ragged_decode_ring") if n != args.workload]:
             cap2 = SOFTCAP_EXAMPLE if name == "prefill_softcap" else None
             real2 = BUCKET_REAL_EXAMPLE if name == "prefill_bucket" else None
             fused2 = not name.startswith("prefill") and not name.endswith("_two_launch")
+            ring2 = RING_EXAMPLE if name == "ragged_decode_ring" else None
             w2, phys2 = workload("prefill" if name.startswith("prefill") else
-                                 name.replace("_two_launch", ""))
+                                 name.replace("_two_launch", "").replace("_ring", ""))
             rot = 12 if name.startswith("e4b_decode") else 1   # e4b inputs rotate past L2
             ms2, lm2, clk2, info2 = timed_graph_run(w2, phys2, args.steps, args.warmup, device,
                                                     world, per_launch=(w2.n_new > 1),
                                                     rotations=rot, softcap=cap2, n_real=real2,
-                                                    fused=fused2)
+                                                    fused=fused2, ring=ring2)
             ms2 = max_over_ranks(ms2, world)
             d2 = w2.n_new == 1
             u2, sc2 = ("GB/s", 1e9) if d2 else ("TFLOP/s", 1e12)
@@ -649,6 +668,9 @@ def run_native(args):
                 ent["softcap"] = cap2
             if real2 is not None:
                 ent["n_real"] = real2
+            if ring2 is not None:
+                ent["ring_slots"] = ring2
+                ent["cache_gb"] = info2["cache_bytes"] / 1e9
             also[name] = ent
         line["also"] = also
     if rank == 0:
