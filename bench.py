@@ -45,8 +45,8 @@ RING_EXAMPLE = 1024      # ring slots of the sliding layers' caches (the 12B win
 # dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
 # captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
 # batch-64 global layer); used only while the kernel sources hash to the recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": "723a40dafacef7b435e19615c10073e117064628",
-                      "per_algorithmic_byte": {"sliding": 1.0197, "global": 1.0376}}
+NCU_DECODE_TRAFFIC = {"source_sha1": "663378c2339e20eff5155d53031455c4c073a056",
+                      "per_algorithmic_byte": {"sliding": 1.0229, "global": 1.0349}}
 
 
 # ---------------------------------------------------------------------------------------------
