@@ -48,6 +48,16 @@
  * model, and its soft-cap value, are not pinned by the pages ("parity
  * unpinned" for them).
  *
+ * Final logits ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", family table and
+ * section 4.2): the model caps its output logits to softcap * tanh(logits / softcap) over the
+ * whole vocabulary (softcap 30, 262,144 tokens), and the page notes that the argmax of the
+ * capped logits is the argmax of the raw ones, so greedy decoding does not depend on the cap.
+ * Reading taken: the greedy index is the argmax of the raw logits (an exact comparison, no
+ * rounding decides it), the lowest index among equal maxima, NaN entries never selected (a row
+ * of NaN gives index 0). Pins: the capped value by its closed forms (a cap far above the logits
+ * changes nothing, saturated logits become +-c, odd symmetry), the index against the first
+ * maximum of numpy and against the argmax of the fp64 capped values (the page's statement).
+ *
  * ORACLE_MUTANT, when defined, plants one deliberate mistake; the test suite
  * builds such variants to show that its pins catch each of them. The normal
  * build never defines it.
@@ -284,4 +294,43 @@ int oracle_attention(const oracle_layer* layers, const int32_t* owner_map, int n
 {
     return oracle_attention_softcap(layers, owner_map, n_layers, layer, k_cache, v_cache, dtype,
                                     capacity, q, n_tok, seq_lens, batch, scale, 0.0, out);
+}
+
+/* Final-logit soft-cap and greedy argmax of each row of logits [batch][vocab] (bf16 or fp32).
+ * capped (optional, [batch][vocab]) receives c * tanh(x / c) for c > 0, x itself for c == 0;
+ * index[b] receives the lowest i with x_i >= x_j for every non-NaN x_j (0 for a row of NaN). */
+int oracle_logit_softcap_argmax(const void* logits, int dtype, int batch, int vocab,
+                                double softcap, double* capped, int32_t* index)
+{
+    if (!logits || !index || batch < 0 || vocab < 1 || !(softcap >= 0.0)) return ORACLE_ERR_ARG;
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP32) return ORACLE_ERR_ARG;
+    for (int b = 0; b < batch; ++b) {
+        int best_i = -1;
+        double best = 0.0;
+        for (int i = 0; i < vocab; ++i) {
+            const double x = load_elem(logits, (size_t)b * vocab + i, dtype);
+            if (capped) {
+                double c = x;
+                if (softcap > 0.0) {
+#if ORACLE_MUTANT == 10
+                    c = softcap * tanh(x);          /* planted: the division by the cap dropped */
+#else
+                    c = softcap * tanh(x / softcap);
+#endif
+                }
+                capped[(size_t)b * vocab + i] = c;
+            }
+            if (isnan(x)) continue;
+#if ORACLE_MUTANT == 9
+            if (best_i < 0 || x >= best) {          /* planted: the last of equal maxima wins */
+#else
+            if (best_i < 0 || x > best) {
+#endif
+                best = x;
+                best_i = i;
+            }
+        }
+        index[b] = best_i < 0 ? 0 : best_i;
+    }
+    return ORACLE_OK;
 }

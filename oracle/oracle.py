@@ -86,6 +86,10 @@ class Oracle:
         lib.oracle_resolve_owner.restype = ctypes.c_int
         lib.oracle_resolve_owner.argtypes = [ctypes.POINTER(_Layer), ctypes.POINTER(ctypes.c_int32),
                                              ctypes.c_int, ctypes.c_int]
+        lib.oracle_logit_softcap_argmax.restype = ctypes.c_int
+        lib.oracle_logit_softcap_argmax.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
         lib.oracle_mutant.restype = ctypes.c_int
         self.lib = lib
         self.mutant = lib.oracle_mutant()
@@ -139,6 +143,21 @@ class Oracle:
         if st != 0:
             raise OracleError(f"oracle_attention status {st}")
         return out
+
+    def logit_softcap_argmax(self, logits: torch.Tensor, softcap: float):
+        """logits [B][V] (bf16 or fp32). Returns (capped fp64 [B][V], index int32 [B]): capped
+        = softcap * tanh(x / softcap) (x when softcap == 0), index = the lowest argmax of the raw
+        logits, NaN never selected."""
+        if logits.dim() != 2:
+            raise OracleError("logits must be [B][V]")
+        B, V = logits.shape
+        capped = torch.empty((B, V), dtype=torch.float64)
+        idx = (ctypes.c_int32 * max(B, 1))()
+        st = self.lib.oracle_logit_softcap_argmax(_ptr(logits), _dtype_code(logits), B, V,
+                                                  float(softcap), _ptr(capped), idx)
+        if st != 0:
+            raise OracleError(f"oracle_logit_softcap_argmax status {st}")
+        return capped, torch.tensor([idx[i] for i in range(B)], dtype=torch.int32)
 
 
 _cached: dict = {}

@@ -256,6 +256,61 @@ def pin_softcap_saturated_scores(orc):
 
 
 # ---------------------------------------------------------------------------------------------
+# the final-logit soft-cap c * tanh(x / c) and the greedy argmax of the raw logits
+# ---------------------------------------------------------------------------------------------
+def pin_logit_cap_closed_forms(orc):
+    """A cap far above the logits changes them by at most |x|^3 / (3 c^2); logits far above the
+    cap become exactly +-c; x = c * atanh(1/2) becomes c / 2; the cap is odd in x."""
+    x = _rand((3, 257), 81) * 4.0
+    capped, _ = orc.logit_softcap_argmax(x, 1.0e6)
+    xd = x.double()
+    assert ((capped - xd).abs() <= xd.abs() ** 3 / (3.0e12) + 1e-15 * (1.0 + xd.abs())).all()
+    c = 30.0
+    sat = torch.tensor([[1.0e4, -1.0e4, 0.0, c * math.atanh(0.5)]], dtype=torch.float32)
+    capped, _ = orc.logit_softcap_argmax(sat, c)
+    assert capped[0, 0].item() == c and capped[0, 1].item() == -c and capped[0, 2].item() == 0.0
+    assert abs(capped[0, 3].item() - c / 2) < 1e-5   # atanh argument rounded to fp32
+    pos, _ = orc.logit_softcap_argmax(x, c)
+    neg, _ = orc.logit_softcap_argmax((-x).contiguous(), c)
+    assert (pos + neg).abs().max().item() < 1e-14
+    plain, _ = orc.logit_softcap_argmax(x, 0.0)
+    assert torch.equal(plain, xd)
+
+
+def pin_logit_argmax_is_first_maximum(orc):
+    """The greedy index equals numpy's argmax (first occurrence of the maximum) on rows with
+    planted equal maxima, in bf16 and fp32."""
+    import numpy as np
+    for dtype in (torch.float32, torch.bfloat16):
+        x = _rand((6, 1000), 82, dtype)
+        for b, (i, j) in enumerate([(3, 900), (0, 999), (500, 501), (7, 8), (998, 999), (1, 2)]):
+            top = x[b].float().max().item() + 1.0
+            x[b, i] = top
+            x[b, j] = top
+        _, idx = orc.logit_softcap_argmax(x, 30.0)
+        ref = np.argmax(x.float().numpy(), axis=1)
+        assert idx.tolist() == ref.tolist()
+
+
+def pin_logit_argmax_ignores_the_cap(orc):
+    """The page's statement: the argmax of the capped logits (fp64, distinct values) is the
+    argmax of the raw logits."""
+    x = _rand((8, 4096), 83) * 6.0
+    capped, idx = orc.logit_softcap_argmax(x, 30.0)
+    assert idx.tolist() == torch.argmax(capped, dim=1).to(torch.int32).tolist()
+    assert idx.tolist() == torch.argmax(x, dim=1).to(torch.int32).tolist()
+
+
+def pin_logit_argmax_nan_and_infinities(orc):
+    """Hand-derived: NaN is never selected; -inf rows pick their first entry; +inf wins."""
+    nan, inf = float("nan"), float("inf")
+    rows = [[nan, -inf, -inf, -inf], [nan, nan, nan, nan], [1.0, nan, 2.0, 2.0],
+            [-inf, 5.0, inf, inf], [-2.0, -1.0, -1.0, -3.0]]
+    _, idx = orc.logit_softcap_argmax(torch.tensor(rows, dtype=torch.float32), 30.0)
+    assert idx.tolist() == [1, 0, 2, 2, 1]
+
+
+# ---------------------------------------------------------------------------------------------
 # invariants
 # ---------------------------------------------------------------------------------------------
 def pin_window_covering_context_is_global(orc):

@@ -3,7 +3,9 @@
 The mistakes are planted in the oracle source behind ORACLE_MUTANT (CPU only):
 1 window edge off by one, 2 scale dropped, 3 interleaved instead of grouped GQA heads,
 4 causal mask dropped, 5 owner map ignored, 6 softmax normaliser over every cached key,
-7 query position without the cached prefix, 8 soft-cap applied to the unscaled score.
+7 query position without the cached prefix, 8 soft-cap applied to the unscaled score,
+9 the last of equal maximal logits taken as the greedy index, 10 logit cap without the
+division by the cap.
 """
 import os
 
@@ -12,7 +14,7 @@ import pytest
 import oracle_pins
 from oracle.oracle import Oracle, OracleError, build_oracle
 
-MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8]
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
