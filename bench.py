@@ -428,6 +428,50 @@ def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rot
     return ms, launch_ms, clk, info
 
 
+def logit_run(steps, warmup, device, world, batch=64, rotations=4):
+    """The greedy step after the LM head: final-logit soft-cap (cap 30, written out) and argmax
+    of [64][262144] bf16 logits, rotating over `rotations` input/output pairs (together larger
+    than L2), each call captured in one graph. Returns time per call and launches per call."""
+    import mixed_sliding_global_gb300 as gemma
+    V = synth.VOCAB
+    xs = [synth.logits(batch, V, seed=r).to(device) for r in range(rotations)]
+    outs = [torch.empty_like(x) for x in xs]
+    idx = torch.empty(batch, dtype=torch.int32, device=device)
+    ws = torch.zeros(max(gemma.gemma_logit_workspace_size(batch, V), 16), dtype=torch.uint8,
+                     device=device)
+
+    def call(r):
+        gemma.gemma_logit_softcap_argmax(xs[r], synth.LOGIT_SOFTCAP, idx, outs[r], ws)
+
+    for r in range(rotations):
+        call(r)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for r in range(rotations):
+            call(r)
+    for _ in range(warmup):
+        g.replay()
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0, t1 = make_event(False), make_event(False)
+    t0.record()
+    for _ in range(steps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / (steps * rotations)
+    n_split = -(-gemma.gemma_logit_workspace_size(batch, V) // (8 * batch))
+    bytes_per_call = batch * V * 2 * 2 + batch * 4
+    del g, xs, outs
+    torch.cuda.empty_cache()
+    return ms, bytes_per_call, 2 if n_split > 1 else 1, clk
+
+
 def e2e_run(w, phys, steps, warmup, device, fused=False):
     """Same step through the public API, eager, with this step's inputs copied from pinned host
     memory and the outputs read back every step (the caches stay resident: they are state)."""
@@ -672,6 +716,17 @@ def run_native(args):
                 ent["ring_slots"] = ring2
                 ent["cache_gb"] = info2["cache_bytes"] / 1e9
             also[name] = ent
+        # the greedy step after the LM head: final-logit soft-cap 30 (capped logits written)
+        # and argmax over the pages' 262,144-token vocabulary, batch 64, bf16
+        lms, lbytes, llaunch, lclk = logit_run(args.steps, args.warmup, device, world)
+        lms = max_over_ranks(lms, world)
+        lv = world * lbytes / (lms * 1e-3) / 1e9
+        also["logit_softcap_argmax"] = {
+            "value": lv, "unit": "GB/s", "ms_per_step": lms, "frac": lv / peaks["hbm_gbs"],
+            "config": {"batch": 64, "vocab": synth.VOCAB, "softcap": synth.LOGIT_SOFTCAP,
+                       "dtype": "bf16", "capped_output": True},
+            "bytes_per_call": lbytes, "gpu_launches_per_step": llaunch,
+            "l2": "4 rotating input/output pairs (268 MB)", "clocks": lclk}
         line["also"] = also
     if rank == 0:
         print(json.dumps(line), flush=True)

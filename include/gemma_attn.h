@@ -260,6 +260,36 @@ int gemma_attn_prefill_bucket(void* out, const void* q, const void* const* k_cac
 size_t gemma_attn_workspace_size(int batch, gemma_layer_kind kind, int window, int n_q,
                                  int n_kv, int head_dim, int max_seq_len, int n_new);
 
+/*
+ * gemma_logit_softcap_argmax -- final-logit soft-cap and greedy argmax of each row.
+ *   capped[b][i] = softcap * tanh(logits[b][i] / softcap)      (logits[b][i] when softcap == 0)
+ *   argmax[b]    = the lowest i with logits[b][i] >= logits[b][j] for every non-NaN j
+ * Source: "Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", family table (logit softcap 30,
+ * vocabulary 262,144) and section 4.2 (the model caps its logits with softcap * tanh(x /
+ * softcap); the argmax of the capped logits is the argmax of the raw ones, so greedy decoding
+ * does not depend on the cap). The index is therefore taken on the raw logits: an exact
+ * comparison, the same in every precision. NaN entries are never selected; a row of NaN gives
+ * index 0. tanh is evaluated with the hardware approximation (relative error below 2^-10).
+ *   logits      DEVICE [batch][vocab] of dtype, row-major, 16-byte aligned (caller-owned).
+ *   capped_out  DEVICE [batch][vocab] of dtype, 16-byte aligned, or NULL to skip the capped
+ *               logits; may equal logits (in place).
+ *   argmax_out  DEVICE int32 [batch].
+ *   softcap     >= 0 and finite.
+ *   workspace   DEVICE scratch of gemma_logit_workspace_size(batch, vocab) bytes, 16-byte
+ *               aligned (NULL when that is 0); holds no state between calls.
+ * Returns GEMMA_ERR_INVALID_ARG (NULL or misaligned pointer, batch < 0, vocab < 1, bad softcap
+ * or dtype), GEMMA_ERR_UNSUPPORTED (batch > 65535) or GEMMA_ERR_WORKSPACE before any launch;
+ * batch == 0 is a no-op. Asynchronous on
+ * `stream`; allocates nothing; graph-capturable.
+ */
+int gemma_logit_softcap_argmax(const void* logits, int batch, int vocab, gemma_dtype dtype,
+                               float softcap, void* capped_out, int32_t* argmax_out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of scratch gemma_logit_softcap_argmax needs on the current device ((size_t)-1 for
+ * batch < 0 or vocab < 1). */
+size_t gemma_logit_workspace_size(int batch, int vocab);
+
 /* A static, human-readable name of a gemma_status value. */
 const char* gemma_status_string(int status);
 

@@ -13,6 +13,6 @@ from .binding import (  # noqa: F401
     gemma_kv_append, gemma_attn_decode, gemma_attn_decode_static, gemma_attn_prefill, gemma_attn_softcap,
     gemma_kv_append_bucket, gemma_attn_prefill_bucket, gemma_attn_decode_append,
     gemma_kv_append_ring,
-    gemma_attn_workspace_size,
+    gemma_attn_workspace_size, gemma_logit_softcap_argmax, gemma_logit_workspace_size,
     gemma_status_string, gemma_abi_version,
 )

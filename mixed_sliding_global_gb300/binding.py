@@ -57,6 +57,10 @@ _SIGNATURES = {
                                            _c_int, _c_float, _c_int, _c_void_p, _c_size_t,
                                            _c_void_p, _c_void_p]),
     "gemma_attn_workspace_size": (_c_size_t, [_c_int] * 8),
+    "gemma_logit_softcap_argmax": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_float,
+                                            _c_void_p, _c_void_p, _c_void_p, _c_size_t,
+                                            _c_void_p]),
+    "gemma_logit_workspace_size": (_c_size_t, [_c_int, _c_int]),
     "gemma_status_string": (ctypes.c_char_p, [_c_int]),
     "gemma_abi_version": (_c_int, []),
 }
@@ -264,6 +268,32 @@ def gemma_attn_workspace_size(batch: int, kind: int, window: int, n_q: int, n_kv
     if n == ctypes.c_size_t(-1).value:
         raise ValueError("invalid arguments for gemma_attn_workspace_size")
     return int(n)
+
+
+def gemma_logit_workspace_size(batch: int, vocab: int) -> int:
+    n = library().gemma_logit_workspace_size(int(batch), int(vocab))
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid arguments for gemma_logit_workspace_size")
+    return int(n)
+
+
+def gemma_logit_softcap_argmax(logits: torch.Tensor, softcap: float, argmax_out: torch.Tensor,
+                               capped_out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """logits, capped_out: [B][V] bf16 or fp32 (capped_out may be logits itself, or None);
+    argmax_out: int32 [B]."""
+    if logits.dim() != 2:
+        raise ValueError("logits must be [B][V]")
+    if argmax_out.dtype != torch.int32:
+        raise TypeError("argmax_out must be int32")
+    B, V = logits.shape
+    ws_ptr = _dev_ptr(workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = library().gemma_logit_softcap_argmax(_dev_ptr(logits), B, V, _dtype(logits),
+                                              float(softcap), _dev_ptr(capped_out),
+                                              _dev_ptr(argmax_out), ws_ptr, ws_bytes,
+                                              _stream(stream))
+    _check("gemma_logit_softcap_argmax", st)
 
 
 def _attn(fn_name, out, q, k_cache, v_cache, owner_map, layer, seq_lens, max_seq_len, n_tok, *,

@@ -6,6 +6,7 @@
 
 #include "../../include/gemma_attn.h"
 #include "attn_internal.h"
+#include "logits.h"
 
 using gemma::RowsParams;
 
@@ -388,6 +389,35 @@ size_t gemma_attn_workspace_size(int batch, gemma_layer_kind kind, int window, i
     const int n_sm = sm_count();
     if (n_sm < 0) return (size_t)-1;
     return make_plan(batch, kind, window, n_q, n_kv, head_dim, max_seq_len, n_new, n_sm).ws_bytes;
+}
+
+int gemma_logit_softcap_argmax(const void* logits, int batch, int vocab, gemma_dtype dtype,
+                               float softcap, void* capped_out, int32_t* argmax_out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    if (batch < 0 || vocab < 1 || (dtype != GEMMA_BF16 && dtype != GEMMA_FP32))
+        return GEMMA_ERR_INVALID_ARG;
+    if (!std::isfinite(softcap) || softcap < 0.f) return GEMMA_ERR_INVALID_ARG;
+    if (batch == 0) return GEMMA_OK;
+    if (batch > 65535) return GEMMA_ERR_UNSUPPORTED;  // one grid row per batch row
+    if (!logits || !argmax_out || !aligned16(logits) || (capped_out && !aligned16(capped_out)))
+        return GEMMA_ERR_INVALID_ARG;
+    const int n_sm = sm_count();
+    if (n_sm < 0) return GEMMA_ERR_CUDA;
+    const gemma::LogitPlan pl = gemma::logit_plan(batch, vocab, n_sm);
+    if (pl.ws_bytes > 0 && (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace)))
+        return GEMMA_ERR_WORKSPACE;
+    const cudaError_t e = gemma::launch_logit_softcap_argmax(
+        logits, capped_out, argmax_out, workspace, batch, vocab, dtype == GEMMA_FP32, softcap, pl,
+        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GEMMA_OK : GEMMA_ERR_CUDA;
+}
+
+size_t gemma_logit_workspace_size(int batch, int vocab) {
+    if (batch < 0 || vocab < 1) return (size_t)-1;
+    if (batch == 0) return 0;
+    const int n_sm = sm_count();
+    if (n_sm < 0) return (size_t)-1;
+    return gemma::logit_plan(batch, vocab, n_sm).ws_bytes;
 }
 
 }  // extern "C"

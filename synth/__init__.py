@@ -159,6 +159,18 @@ def randn(shape, tid: int, dtype: int) -> torch.Tensor:
     return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(TORCH_DTYPE[dtype])
 
 
+# final logits of a greedy step: [batch][vocab], N(0, 8^2) (most values inside the cap of 30,
+# a few beyond it), rounded to the dtype; seeded per call
+LOGIT_SOFTCAP = 30.0
+VOCAB = 262144
+
+
+def logits(batch: int, vocab: int = VOCAB, seed: int = 0, dtype: int = BF16) -> torch.Tensor:
+    g = torch.Generator().manual_seed(BASE_SEED + (1 << 30) + seed)  # apart from tensor ids
+    x = torch.randn((batch, vocab), generator=g, dtype=torch.float32) * 8.0
+    return x.to(torch.bfloat16 if dtype == BF16 else torch.float32)
+
+
 def needed_row_lo(spec: LayerSpec, ctx: int, n_new: int) -> int:
     """First cache row any query of this step may attend: 0 for global layers; for sliding
     layers the oldest window start among the new queries. Rows below it are never read and

@@ -152,3 +152,21 @@ def test_binding_has_no_fallback():
     # every computing entry point of the binding goes through the shared library
     src = open(binding.__file__).read()
     assert "oracle" not in src and "torch.nn.functional" not in src
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, 1, 4, 0, float("nan")), INVALID), ((FAKE, 1, 4, 0, -1.0), INVALID),
+    ((FAKE, 1, 0, 0, 30.0), INVALID), ((FAKE, -1, 4, 0, 30.0), INVALID),
+    ((FAKE, 1, 4, 7, 30.0), INVALID), ((None, 1, 4, 0, 30.0), INVALID),
+    ((FAKE + 8, 1, 4, 0, 30.0), INVALID), ((FAKE, 0, 4, 0, 30.0), 0),
+])
+def test_logit_argument_errors(args, status):
+    """The logit soft-cap / argmax entry point rejects bad arguments on the host."""
+    logits, batch, vocab, dtype, cap = args
+    assert lib().gemma_logit_softcap_argmax(logits, batch, vocab, dtype, cap, None, FAKE, None, 0,
+                                            None) == status
+    assert lib().gemma_logit_softcap_argmax(FAKE, 1, 4, 0, 30.0, FAKE + 4, FAKE, None, 0,
+                                            None) == INVALID   # misaligned capped output
+    assert lib().gemma_logit_workspace_size(-1, 4) == ctypes.c_size_t(-1).value
+    assert lib().gemma_logit_workspace_size(1, 0) == ctypes.c_size_t(-1).value
+    assert lib().gemma_logit_workspace_size(0, 4) == 0
