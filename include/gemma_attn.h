@@ -72,6 +72,7 @@ typedef enum {
 #define GEMMA_DEVERR_WRITE_POS 2u  /* write_pos[b] < 0 or write_pos[b] + n_new > kv_capacity */
 #define GEMMA_DEVERR_TIMEOUT 4u    /* an internal pipeline wait gave up */
 #define GEMMA_DEVERR_N_REAL 8u     /* n_real[b] outside [0, n_new] (padded-bucket entry points) */
+#define GEMMA_DEVERR_PAGE 16u      /* a block-table entry outside [0, n_pages) (paged entry points) */
 
 /*
  * gemma_kv_append -- write this step's new K (and V) rows of an owner layer into its cache.
@@ -259,6 +260,50 @@ int gemma_attn_prefill_bucket(void* out, const void* q, const void* const* k_cac
  */
 size_t gemma_attn_workspace_size(int batch, gemma_layer_kind kind, int window, int n_q,
                                  int n_kv, int head_dim, int max_seq_len, int n_new);
+
+/*
+ * Paged KV pool -- the pages keep one fixed-capacity, device-resident KV buffer per layer,
+ * updated in place (first page, section 5.1; "Gemma-4-E4B-it on AWS Inferentia2", "Decode
+ * neff"). These entry points store the same logical cache of each owner layer in a shared pool
+ * of fixed-size pages instead, so that a ragged batch holds only the pages its sequences use:
+ *   pool        DEVICE [n_pages][n_kv][page_size][head_dim] per owner layer (k_pool[l], and
+ *               v_pool[l] unless k_eq_v), caller-owned, 16-byte aligned.
+ *   block_table DEVICE int32 [batch][max_pages]: position p of sequence b lives in page
+ *               block_table[b * max_pages + p / page_size], row p % page_size. The same table
+ *               may serve every layer. Entries are read only for the pages that hold keys a
+ *               step attends or writes (from the window start rounded down to a multiple of 32
+ *               keys, 128 for prefill, to the last position), so pages wholly before a sliding
+ *               window may be recycled by the caller. An entry outside [0, n_pages) that is read
+ *               sets GEMMA_DEVERR_PAGE; its rows read as zeros and are never written.
+ *   page_size   a multiple of 128 (GEMMA_ERR_UNSUPPORTED otherwise): no key tile crosses a page.
+ * The logical capacity of a sequence is max_pages * page_size; every other argument, the
+ * definitions and the error behaviour are those of gemma_kv_append / gemma_attn_decode /
+ * gemma_attn_prefill. Kinds GEMMA_SLIDING and GEMMA_GLOBAL only.
+ */
+int gemma_kv_append_paged(void* const* k_pool, void* const* v_pool, const int32_t* owner_map,
+                          int n_layers, int layer, const void* k_new, const void* v_new,
+                          const int32_t* write_pos, const int32_t* block_table, int max_pages,
+                          int page_size, int n_pages, int batch, int n_new, int n_kv,
+                          int head_dim, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
+                          void* stream);
+
+/* Attention over a paged pool: a decode step (n_new == 1) or a prefill bucket (n_new > 1).
+ * With k_new != NULL (decode only, owner layers) the launch first writes this step's K (and V)
+ * row [batch][1][n_kv][head_dim] at write_pos[b], as gemma_attn_decode_append does. Scratch:
+ * gemma_attn_workspace_size_paged(...) bytes. */
+int gemma_attn_paged(void* out, const void* q, void* const* k_pool, void* const* v_pool,
+                     const int32_t* owner_map, int n_layers, int layer, const int32_t* seq_lens,
+                     const int32_t* block_table, int max_pages, int page_size, int n_pages,
+                     int max_seq_len, int n_new, int batch, gemma_layer_kind kind, int window,
+                     int n_q, int n_kv, int head_dim, int k_eq_v, float scale, gemma_dtype dtype,
+                     const void* k_new, const void* v_new, const int32_t* write_pos,
+                     void* workspace, size_t workspace_bytes, uint32_t* device_error,
+                     void* stream);
+
+/* Scratch bytes of gemma_attn_paged for these arguments on the current device ((size_t)-1 for
+ * invalid arguments, including GEMMA_SLIDING_RING). */
+size_t gemma_attn_workspace_size_paged(int batch, gemma_layer_kind kind, int window, int n_q,
+                                       int n_kv, int head_dim, int max_seq_len, int n_new);
 
 /*
  * gemma_logit_softcap_argmax -- final-logit soft-cap and greedy argmax of each row.

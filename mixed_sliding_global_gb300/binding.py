@@ -15,6 +15,7 @@ GEMMA_BF16, GEMMA_FP32 = 0, 1
 GEMMA_OK = 0
 GEMMA_DEVERR_SEQ_LEN, GEMMA_DEVERR_WRITE_POS, GEMMA_DEVERR_TIMEOUT = 1, 2, 4
 GEMMA_DEVERR_N_REAL = 8
+GEMMA_DEVERR_PAGE = 16
 
 _c_int, _c_void_p, _c_size_t, _c_float = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
 _PVOID = ctypes.POINTER(ctypes.c_void_p)
@@ -57,6 +58,17 @@ _SIGNATURES = {
                                            _c_int, _c_float, _c_int, _c_void_p, _c_size_t,
                                            _c_void_p, _c_void_p]),
     "gemma_attn_workspace_size": (_c_size_t, [_c_int] * 8),
+    "gemma_kv_append_paged": (_c_int, [_PVOID, _PVOID, _PI32, _c_int, _c_int, _c_void_p,
+                                       _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                       _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p,
+                                       _c_void_p]),
+    "gemma_attn_paged": (_c_int, [_c_void_p, _c_void_p, _PVOID, _PVOID, _PI32, _c_int, _c_int,
+                                  _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                  _c_float, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                  _c_size_t, _c_void_p, _c_void_p]),
+    "gemma_attn_workspace_size_paged": (_c_size_t, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                                    _c_int, _c_int, _c_int]),
     "gemma_logit_softcap_argmax": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_float,
                                             _c_void_p, _c_void_p, _c_void_p, _c_size_t,
                                             _c_void_p]),
@@ -267,6 +279,61 @@ def gemma_attn_workspace_size(batch: int, kind: int, window: int, n_q: int, n_kv
                                             n_new)
     if n == ctypes.c_size_t(-1).value:
         raise ValueError("invalid arguments for gemma_attn_workspace_size")
+    return int(n)
+
+
+def gemma_kv_append_paged(k_pool: Sequence[Optional[torch.Tensor]],
+                          v_pool: Optional[Sequence[Optional[torch.Tensor]]], owner_map,
+                          layer: int, k_new: torch.Tensor, v_new: Optional[torch.Tensor],
+                          write_pos: torch.Tensor, block_table: torch.Tensor, *, k_eq_v: bool,
+                          device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k_pool[l], v_pool[l]: [n_pages][n_kv][page_size][d]; k_new, v_new: [B][n_new][n_kv][d];
+    block_table: int32 [B][max_pages]."""
+    n_layers = len(owner_map)
+    kp = _cache_of(k_pool, owner_map, layer)
+    n_pages, _, page_size, d = kp.shape
+    B, n_new, n_kv, _ = k_new.shape
+    vps = list(v_pool) if v_pool is not None else [None] * n_layers
+    st = library().gemma_kv_append_paged(
+        _ptr_array(list(k_pool)), _ptr_array(vps), _i32_array(owner_map), n_layers, layer,
+        _dev_ptr(k_new), _dev_ptr(v_new), _dev_ptr(write_pos), _dev_ptr(block_table),
+        int(block_table.shape[1]), int(page_size), int(n_pages), B, n_new, n_kv, d,
+        int(bool(k_eq_v)), _dtype(k_new), _dev_ptr(device_error), _stream(stream))
+    _check("gemma_kv_append_paged", st)
+
+
+def gemma_attn_paged(out: torch.Tensor, q: torch.Tensor, k_pool, v_pool, owner_map, layer: int,
+                     seq_lens: torch.Tensor, block_table: torch.Tensor, max_seq_len: int, *,
+                     kind: int, window: int, n_kv: int, k_eq_v: bool, scale: float,
+                     k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                     write_pos: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None,
+                     device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q, out: [B][n_new][n_q][d]; pools per layer [n_pages][n_kv][page_size][d]; block_table
+    int32 [B][max_pages]; k_new/v_new/write_pos: the fused append of a decode step."""
+    n_layers = len(owner_map)
+    kp = _cache_of(k_pool, owner_map, layer)
+    n_pages, _, page_size, _ = kp.shape
+    B, n_tok, n_q, d = q.shape
+    vps = list(v_pool) if v_pool is not None else [None] * n_layers
+    ws_ptr = _dev_ptr(workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = library().gemma_attn_paged(
+        _dev_ptr(out), _dev_ptr(q), _ptr_array(list(k_pool)), _ptr_array(vps),
+        _i32_array(owner_map), n_layers, layer, _dev_ptr(seq_lens), _dev_ptr(block_table),
+        int(block_table.shape[1]), int(page_size), int(n_pages), int(max_seq_len), n_tok, B,
+        int(kind), int(window), n_q, int(n_kv), d, int(bool(k_eq_v)), float(scale), _dtype(q),
+        _dev_ptr(k_new), _dev_ptr(v_new), _dev_ptr(write_pos), ws_ptr, ws_bytes,
+        _dev_ptr(device_error), _stream(stream))
+    _check("gemma_attn_paged", st)
+
+
+def gemma_attn_workspace_size_paged(batch: int, kind: int, window: int, n_q: int, n_kv: int,
+                                    head_dim: int, max_seq_len: int, n_new: int = 1) -> int:
+    n = library().gemma_attn_workspace_size_paged(batch, kind, window, n_q, n_kv, head_dim,
+                                                  max_seq_len, n_new)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid arguments for gemma_attn_workspace_size_paged")
     return int(n)
 
 

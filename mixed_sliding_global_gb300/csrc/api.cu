@@ -71,14 +71,14 @@ struct Plan {
 // least kMinChunkKeys keys each) for large ones. Prefill has one row tile per 16 rows and no
 // split. Depends only on the arguments and the SM count.
 Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim, int max_seq_len,
-               int n_tok, int n_sm) {
+               int n_tok, int n_sm, bool paged = false) {
     Plan pl{1, 1 << 30, 0, 0};
     if (n_tok != 1) return pl;
     const long long T = gemma::kKeyTile;
     long long n_read = kind != GEMMA_GLOBAL && window < max_seq_len ? window : max_seq_len;
-    // a ring cache's key tiles start at multiples of the tile (so that none wraps): up to T - 1
-    // keys before the window join the range
-    if (kind == GEMMA_SLIDING_RING) n_read += T - 1;
+    // a ring cache's or paged pool's key tiles start at multiples of the tile (so that none wraps
+    // or crosses a page): up to T - 1 keys before the window join the range
+    if (kind == GEMMA_SLIDING_RING || paged) n_read += T - 1;
     const long long total = (long long)batch * n_kv * n_read;
     const long long one_per_sm = round_up((total + n_sm - 1) / n_sm, T);
     const long long eight_per_sm =
@@ -106,8 +106,20 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
               int head_dim, int k_eq_v, int kv_capacity, float scale, float softcap, int dtype,
               void* workspace, size_t workspace_bytes, uint32_t* device_error, void* stream,
               const int32_t* n_real = nullptr, const void* k_new = nullptr,
-              const void* v_new = nullptr, const int32_t* write_pos = nullptr) {
+              const void* v_new = nullptr, const int32_t* write_pos = nullptr,
+              const gemma::PagedLayout* pg = nullptr) {
     if (batch < 0 || n_tok < 1) return GEMMA_ERR_INVALID_ARG;
+    if (pg) {  // paged pool: a multiple of 128 keys per page, so that no key tile crosses a page
+        if (kind == GEMMA_SLIDING_RING || pg->page_size < 128 || pg->page_size % 128 != 0 ||
+            pg->max_pages < 1 || pg->n_pages < 1)
+            return pg->page_size > 0 && pg->page_size % 128 != 0 ? GEMMA_ERR_UNSUPPORTED
+                                                                  : GEMMA_ERR_INVALID_ARG;
+        if ((long long)pg->max_pages * pg->page_size > (1ll << 30) ||
+            (long long)pg->n_pages * n_kv > (1ll << 31) - 1)
+            return GEMMA_ERR_UNSUPPORTED;
+        if (batch > 0 && !pg->block_table) return GEMMA_ERR_INVALID_ARG;
+        kv_capacity = pg->max_pages * pg->page_size;  // logical capacity of a sequence
+    }
     if (!std::isfinite(softcap) || softcap < 0.f) return GEMMA_ERR_INVALID_ARG;
     int st = check_shape(kind, window, n_q, n_kv, head_dim, dtype);
     if (st != GEMMA_OK) return st;
@@ -139,7 +151,7 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     // a padded bucket is never split over keys (pad rows have no key range to merge)
     const Plan pl = n_real ? Plan{1, 1 << 30, 0, 0}
                            : make_plan(batch, kind, window, n_q, n_kv, head_dim, max_seq_len,
-                                       n_tok, n_sm);
+                                       n_tok, n_sm, pg != nullptr);
     if (pl.ws_bytes > 0 &&
         (!workspace || workspace_bytes < pl.ws_bytes || !aligned16(workspace)))
         return GEMMA_ERR_WORKSPACE;
@@ -167,6 +179,12 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     p.window = window;
     p.is_sliding = kind != GEMMA_GLOBAL;
     p.ring = ring ? kv_capacity : 0;
+    if (pg) {
+        p.block_table = pg->block_table;
+        p.page_size = pg->page_size;
+        p.max_pages = pg->max_pages;
+        p.n_pages = pg->n_pages;
+    }
     p.k_eq_v = k_eq_v ? 1 : 0;
     p.max_seq_len = max_seq_len;
     p.n_split = pl.n_split;
@@ -200,7 +218,8 @@ int append_rows(void* const* k_cache, void* const* v_cache, const int32_t* owner
                 int n_layers, int layer, const void* k_new, const void* v_new,
                 const int32_t* write_pos, const int32_t* n_real, int ring, int batch, int n_new,
                 int n_kv, int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
-                uint32_t* device_error, void* stream);
+                uint32_t* device_error, void* stream,
+                const gemma::PagedLayout& pg = gemma::PagedLayout{nullptr, 0, 0, 0});
 
 }  // namespace
 
@@ -259,7 +278,7 @@ int append_rows(void* const* k_cache, void* const* v_cache, const int32_t* owner
                 int n_layers, int layer, const void* k_new, const void* v_new,
                 const int32_t* write_pos, const int32_t* n_real, int ring, int batch, int n_new,
                 int n_kv, int head_dim, int kv_capacity, int k_eq_v, gemma_dtype dtype,
-                uint32_t* device_error, void* stream) {
+                uint32_t* device_error, void* stream, const gemma::PagedLayout& pg) {
     if (batch < 0 || n_new < 0 || n_kv < 1 || kv_capacity < 1) return GEMMA_ERR_INVALID_ARG;
     if (dtype != GEMMA_BF16 && dtype != GEMMA_FP32) return GEMMA_ERR_INVALID_ARG;
     if (!head_dim_ok(head_dim)) return GEMMA_ERR_UNSUPPORTED;
@@ -282,7 +301,7 @@ int append_rows(void* const* k_cache, void* const* v_cache, const int32_t* owner
     if (n_sm < 0) return GEMMA_ERR_CUDA;
     const int row_bytes = head_dim * (dtype == GEMMA_BF16 ? 2 : 4);
     cudaError_t e = gemma::launch_kv_append(k_cache[layer], vc, k_new, vc ? v_new : nullptr,
-                                            write_pos, n_real, ring, batch, n_new, n_kv,
+                                            write_pos, n_real, ring, pg, batch, n_new, n_kv,
                                             kv_capacity,
                                             row_bytes, device_error, n_sm,
                                             static_cast<cudaStream_t>(stream));
@@ -365,6 +384,82 @@ int gemma_attn_decode_append(void* out, const void* q, void* const* k_cache, voi
                      kind, window, n_q, n_kv, head_dim, k_eq_v, kv_capacity, scale, 0.f, dtype,
                      workspace, workspace_bytes, device_error, stream, nullptr, k_new,
                      k_eq_v ? nullptr : v_new, write_pos);
+}
+
+namespace {
+int check_paged(int max_pages, int page_size, int n_pages) {
+    if (page_size > 0 && page_size % 128 != 0) return GEMMA_ERR_UNSUPPORTED;
+    if (page_size < 128 || max_pages < 1 || n_pages < 1) return GEMMA_ERR_INVALID_ARG;
+    if ((long long)max_pages * page_size > (1ll << 30)) return GEMMA_ERR_UNSUPPORTED;
+    return GEMMA_OK;
+}
+}  // namespace
+
+int gemma_kv_append_paged(void* const* k_pool, void* const* v_pool, const int32_t* owner_map,
+                          int n_layers, int layer, const void* k_new, const void* v_new,
+                          const int32_t* write_pos, const int32_t* block_table, int max_pages,
+                          int page_size, int n_pages, int batch, int n_new, int n_kv,
+                          int head_dim, int k_eq_v, gemma_dtype dtype, uint32_t* device_error,
+                          void* stream) {
+    const int st = check_paged(max_pages, page_size, n_pages);
+    if (st != GEMMA_OK) return st;
+    if (batch > 0 && n_new > 0 && !block_table) return GEMMA_ERR_INVALID_ARG;
+    const gemma::PagedLayout pg{block_table, max_pages, page_size, n_pages};
+    return append_rows(k_pool, v_pool, owner_map, n_layers, layer, k_new, v_new, write_pos,
+                       nullptr, 0, batch, n_new, n_kv, head_dim, max_pages * page_size, k_eq_v,
+                       dtype, device_error, stream, pg);
+}
+
+int gemma_attn_paged(void* out, const void* q, void* const* k_pool, void* const* v_pool,
+                     const int32_t* owner_map, int n_layers, int layer, const int32_t* seq_lens,
+                     const int32_t* block_table, int max_pages, int page_size, int n_pages,
+                     int max_seq_len, int n_new, int batch, gemma_layer_kind kind, int window,
+                     int n_q, int n_kv, int head_dim, int k_eq_v, float scale, gemma_dtype dtype,
+                     const void* k_new, const void* v_new, const int32_t* write_pos,
+                     void* workspace, size_t workspace_bytes, uint32_t* device_error,
+                     void* stream) {
+    if (n_new == 0 && batch >= 0) return GEMMA_OK;
+    int st = check_paged(max_pages, page_size, n_pages);
+    if (st != GEMMA_OK) return st;
+    const gemma::PagedLayout pg{block_table, max_pages, page_size, n_pages};
+    const void* const* kcc = const_cast<const void* const*>(k_pool);
+    const void* const* vcc = const_cast<const void* const*>(v_pool);
+    int o = 0;
+    st = resolve_owner(owner_map, n_layers, layer, &o);
+    if (st != GEMMA_OK) return st;
+    if (k_new && o == layer) {  // this step's rows are written by the decode launch itself
+        if (n_new != 1) return GEMMA_ERR_INVALID_ARG;
+        if (batch > 0 && (!write_pos || (!k_eq_v && !v_new))) return GEMMA_ERR_INVALID_ARG;
+        if (batch > 0 && (!aligned16(k_new) || (!k_eq_v && !aligned16(v_new))))
+            return GEMMA_ERR_INVALID_ARG;
+        if (dtype != GEMMA_BF16) {  // the fp32 debug path: append, then attend
+            st = append_rows(k_pool, v_pool, owner_map, n_layers, layer, k_new, v_new, write_pos,
+                             nullptr, 0, batch, 1, n_kv, head_dim, max_pages * page_size, k_eq_v,
+                             dtype, device_error, stream, pg);
+            if (st != GEMMA_OK) return st;
+        } else {
+            return attention(out, q, kcc, vcc, owner_map, n_layers, layer, seq_lens, max_seq_len,
+                             1, batch, kind, window, n_q, n_kv, head_dim, k_eq_v, 0, scale, 0.f,
+                             dtype, workspace, workspace_bytes, device_error, stream, nullptr,
+                             k_new, k_eq_v ? nullptr : v_new, write_pos, &pg);
+        }
+    }
+    return attention(out, q, kcc, vcc, owner_map, n_layers, layer, seq_lens, max_seq_len, n_new,
+                     batch, kind, window, n_q, n_kv, head_dim, k_eq_v, 0, scale, 0.f, dtype,
+                     workspace, workspace_bytes, device_error, stream, nullptr, nullptr, nullptr,
+                     nullptr, &pg);
+}
+
+size_t gemma_attn_workspace_size_paged(int batch, gemma_layer_kind kind, int window, int n_q,
+                                       int n_kv, int head_dim, int max_seq_len, int n_new) {
+    if (batch < 0 || n_new < 1 || max_seq_len < n_new || kind == GEMMA_SLIDING_RING)
+        return (size_t)-1;
+    if (check_shape(kind, window, n_q, n_kv, head_dim, GEMMA_BF16) != GEMMA_OK) return (size_t)-1;
+    if (batch == 0) return 0;
+    const int n_sm = sm_count();
+    if (n_sm < 0) return (size_t)-1;
+    return make_plan(batch, kind, window, n_q, n_kv, head_dim, max_seq_len, n_new, n_sm, true)
+        .ws_bytes;
 }
 
 int gemma_attn_prefill_bucket(void* out, const void* q, const void* const* k_cache,

@@ -29,6 +29,10 @@ struct RowsParams {
     int n_tok, n_q, n_kv, G, cap, window, is_sliding, k_eq_v;
     int max_seq_len;
     int ring;                 // ring cache of this many slots (position p at p % ring), or 0
+    // paged pool [n_pages][n_kv][page_size][D] (page_size > 0): position p of sequence b lives
+    // in page block_table[b][p / page_size], row p % page_size; cap = max_pages * page_size
+    const int32_t* block_table;
+    int page_size, max_pages, n_pages;
     int n_split;              // key chunks per row tile (1: write `out` directly)
     int chunk;                // keys per chunk (multiple of the key tile)
     int n_stages;             // smem pipeline depth (bf16 kernel)
@@ -41,6 +45,30 @@ struct RowsParams {
     float cap_inner;
     float cap_log2;
 };
+
+#ifdef __CUDACC__
+// Row of the [rows][slots][D] view of the cache that the tensor maps and direct accesses use,
+// and slot, of key `key` of sequence b and KV head kvh: row b * n_kv + kvh and slot key (key %
+// ring for a ring cache); for a paged pool row page * n_kv + kvh and slot key % page_size, page
+// the sequence's block-table entry. Returns false for a page index outside [0, n_pages).
+__device__ __forceinline__ bool kv_place(const RowsParams& p, int b, int kvh, int key, int& row,
+                                         int& slot) {
+    if (p.page_size) {
+        const int blk = key / p.page_size;
+        const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + blk);
+        row = pg * p.n_kv + kvh;
+        slot = key - blk * p.page_size;
+        return pg >= 0 && pg < p.n_pages;
+    }
+    row = b * p.n_kv + kvh;
+    slot = p.ring ? key % p.ring : key;
+    return true;
+}
+// slots per row of that view
+__device__ __forceinline__ int kv_row_slots(const RowsParams& p) {
+    return p.page_size ? p.page_size : p.cap;
+}
+#endif
 
 // Keys per shared-memory tile of the bf16 kernel; chunks are multiples of it.
 constexpr int kKeyTile = 32;
@@ -55,8 +83,14 @@ cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out
                            cudaStream_t st);
 bool prefill_tc_supported(int head_dim);
 cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cudaStream_t st);
+// paged pool layout for the append (block_table == nullptr: a plain or ring cache)
+struct PagedLayout {
+    const int32_t* block_table;
+    int max_pages, page_size, n_pages;
+};
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                              const int32_t* write_pos, const int32_t* n_real, int ring,
+                             const PagedLayout& pg,
                              int batch, int n_new, int n_kv,
                              int capacity, int row_bytes, uint32_t* err, int n_sm,
                              cudaStream_t st);

@@ -2,7 +2,9 @@
 //
 //   cache[b][h][write_pos[b] + t][:] = new[b][t][h][:]     for t < n_real[b] (all n_new rows
 //                                                           when n_real is null)
-// and, into a ring cache of R slots, at slot (write_pos[b] + t) % R.
+// and, into a ring cache of R slots, at slot (write_pos[b] + t) % R; into a paged pool
+// [n_pages][n_kv][page_size][D], position p = write_pos[b] + t goes to page
+// block_table[b][p / page_size], row p % page_size.
 //
 // "Gemma-4-E4B-it on AWS Inferentia2" ("Decode neff") keeps the KV buffers on the device and
 // updates them in place each step; its one-hot masked write exists only to keep a traced
@@ -20,7 +22,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
                                                         const uint8_t* __restrict__ vn,
                                                         const int32_t* __restrict__ write_pos,
                                                         const int32_t* __restrict__ n_real,
-                                                        int ring, int batch, int n_new, int n_kv,
+                                                        int ring, const PagedLayout pg,
+                                                        int batch, int n_new, int n_kv,
                                                         int capacity, int row_bytes,
                                                         uint32_t* err) {
     const int chunks = row_bytes / 16;
@@ -44,9 +47,21 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
             if (t == 0 && h == 0 && ch == 0) report(err, GEMMA_DEVERR_WRITE_POS);
             continue;
         }
-        const long long slot = ring ? ((long long)pos + t) % ring : (long long)pos + t;
-        const size_t dst = (((size_t)b * n_kv + h) * (size_t)capacity + (size_t)slot) *
-                               (size_t)row_bytes + (size_t)ch * 16;
+        size_t dst;
+        if (pg.block_table) {  // capacity = max_pages * page_size
+            const int p_abs = pos + t, blk = p_abs / pg.page_size;
+            const int page = __ldg(pg.block_table + (size_t)b * pg.max_pages + blk);
+            if (page < 0 || page >= pg.n_pages) {
+                if (h == 0 && ch == 0) report(err, GEMMA_DEVERR_PAGE);
+                continue;
+            }
+            dst = (((size_t)page * n_kv + h) * (size_t)pg.page_size +
+                   (size_t)(p_abs - blk * pg.page_size)) * (size_t)row_bytes + (size_t)ch * 16;
+        } else {
+            const long long slot = ring ? ((long long)pos + t) % ring : (long long)pos + t;
+            dst = (((size_t)b * n_kv + h) * (size_t)capacity + (size_t)slot) *
+                      (size_t)row_bytes + (size_t)ch * 16;
+        }
         const size_t src = (size_t)row * row_bytes + (size_t)ch * 16;
         *reinterpret_cast<uint4*>(kc + dst) = __ldg(reinterpret_cast<const uint4*>(kn + src));
         if (vc) *reinterpret_cast<uint4*>(vc + dst) = __ldg(reinterpret_cast<const uint4*>(vn + src));
@@ -55,6 +70,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                              const int32_t* write_pos, const int32_t* n_real, int ring,
+                             const PagedLayout& pg,
                              int batch, int n_new, int n_kv, int capacity, int row_bytes,
                              uint32_t* err, int n_sm, cudaStream_t st) {
     const long long total = (long long)batch * n_new * n_kv * (row_bytes / 16);
@@ -65,7 +81,7 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, co
     kv_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(
         static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
         static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), write_pos, n_real,
-        ring, batch, n_new, n_kv, capacity, row_bytes, err);
+        ring, pg, batch, n_new, n_kv, capacity, row_bytes, err);
     return cudaGetLastError();
 }
 

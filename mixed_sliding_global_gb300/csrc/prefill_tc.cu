@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int pos_first = len - n_real + tok_first, pos_last = len - n_real + tok_last;
     // (a ring cache's tiles start at multiples of the tile, so that none wraps around the ring;
     // the rows' masks drop the keys before the window)
-    const int k_begin = p.is_sliding ? (max(0, pos_first - p.window + 1) & (p.ring ? ~(kTcKeys - 1) : ~0))
+    const int k_begin = p.is_sliding ? (max(0, pos_first - p.window + 1) & ((p.ring || p.page_size) ? ~(kTcKeys - 1) : ~0))
                                      : 0;
     const int k_end = pos_last + 1;
     const int n_tiles = n_rows_real == 0 ? 0 : (k_end - k_begin + kTcKeys - 1) / kTcKeys;
@@ -212,12 +212,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // K tiles use slots [0, NK), V tiles slots [NK, NS). K runs one tile ahead of V, so a
         // K slot is refilled as soon as its S = Q K^T finished, independently of P V.
         if (lane == 0) {
-            const int row3 = b * p.n_kv + kvh;
             auto load = [&](const CUtensorMap* map, int slot, int t) {
                 uint8_t* dst = slots + slot * Lay::SLOT;
                 mbar_arrive_expect_tx(&kv_full[slot], Lay::SLOT);
-                const int key0 = k_begin + t * kTcKeys;
-                const int slot0 = p.ring ? key0 % p.ring : key0;  // cache slot of the first key
+                // cache row and slot of the tile's first key (a bad page index reads zeros)
+                int row3 = 0, slot0 = 0;
+                if (!kv_place(p, b, kvh, k_begin + t * kTcKeys, row3, slot0)) {
+                    report(p.err, GEMMA_DEVERR_PAGE);
+                    row3 = p.n_pages * p.n_kv;
+                }
                 for (int c = 0; c < Lay::CHUNKS; ++c)
                     tma_load_3d(dst + c * kTcKeys * 128, map, (int)h * DH + c * 64, slot0, row3,
                                 &kv_full[slot]);
@@ -256,6 +259,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t id_qk = idesc_bf16(128, kTcKeys, 0, 0);
         const uint32_t id_pv = idesc_bf16(128, DH, 0, 1);
         bool ok = mbar_wait(q_ready, 0, p.err);
+        // rows [0, n_head) of the first tile when it starts before every row's window (a
+        // tile-aligned start): masked keys whose values must not reach P V as 0 * x
+        const int n_head = p.is_sliding ? max(0, max(0, pos_first - p.window + 1) - k_begin) : 0;
+        auto zero_head = [&](uint8_t* tile) {
+            for (int idx = lane; idx < Lay::CHUNKS * n_head * 8; idx += 32) {
+                const int c = idx / (n_head * 8), rem = idx - c * n_head * 8;
+                *reinterpret_cast<uint4*>(tile + c * kTcKeys * 128 + (rem / 8) * 128 +
+                                          (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        };
         auto zero_tail = [&](uint8_t* tile, int n_valid) {
             // rows [n_valid, 128) of every 64-column box: whole 128-byte rows, so the
             // swizzle does not matter
@@ -285,6 +300,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = mbar_wait(&kv_full[sv], sv_phase, p.err);
                 const int n_valid = k_end - (k_begin + j * kTcKeys);
                 if (n_valid < kTcKeys) zero_tail(slots + sv * Lay::SLOT, n_valid);
+                if (j == 0 && n_head > 0) zero_head(slots + sv * Lay::SLOT);
             }
             tc_fence_after();
             if (lane == 0) {
@@ -312,6 +328,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (p.k_eq_v) {
                 const int n_valid = k_end - (k_begin + t * kTcKeys);
                 if (n_valid < kTcKeys) zero_tail(slots + sk * Lay::SLOT, n_valid);
+                if (t == 0 && n_head > 0) zero_head(slots + sk * Lay::SLOT);
             }
             if (t >= 1 && ok) ok = mbar_wait(s_free, (t - 1) & 1, p.err);
             tc_fence_after();
@@ -545,8 +562,11 @@ template <int D, int CL>
 static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
     using Lay = TcLayout<D, CL>;
     CUtensorMap km, vm;
-    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.cap, (uint64_t)batch * p.n_kv};
-    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.cap * D * 2};
+    // [rows][slots][D]: rows = sequences x KV heads (pages x KV heads for a paged pool)
+    const uint64_t map_slots = p.page_size ? (uint64_t)p.page_size : (uint64_t)p.cap;
+    const uint64_t map_rows = p.page_size ? (uint64_t)p.n_pages * p.n_kv : (uint64_t)batch * p.n_kv;
+    const uint64_t dims[3] = {(uint64_t)D, map_slots, map_rows};
+    const uint64_t strides[2] = {(uint64_t)D * 2, map_slots * D * 2};
     const uint32_t box[3] = {64, (uint32_t)kTcKeys, 1};
     if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;

@@ -126,9 +126,9 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     // keys any row of this tile may attend, then this CTA's chunk of them
     const RowInfo first = row_info(p, len, kvh, row0);
     const RowInfo last = row_info(p, len, kvh, row0 + n_rows - 1);
-    // a ring cache's chunks start at multiples of the key tile, so that no tile wraps around the
-    // ring (the rows' masks drop the keys before the window)
-    const int base = p.ring ? (first.lo & ~(T - 1)) : first.lo;
+    // a ring cache's or paged pool's chunks start at multiples of the key tile, so that no tile
+    // wraps around the ring or crosses a page (the rows' masks drop the keys before the window)
+    const int base = (p.ring || p.page_size) ? (first.lo & ~(T - 1)) : first.lo;
     const int kb = base + split * p.chunk;
     const int ke = min(last.pos + 1, kb + p.chunk);
     if (kb >= ke) return;  // empty chunk: the combine pass skips it
@@ -185,13 +185,15 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
             const bool in_range = wp >= first.lo && wp <= last.pos;
             const bool writer = rt == 0 && (in_range ? (wp >= kb && wp < ke) : split == 0);
             if (writer) {
+                int wrow = 0, wslot = 0;
                 if (wp < 0 || (!p.ring && wp >= p.cap)) {
                     if (lane == 0) report(p.err, GEMMA_DEVERR_WRITE_POS);
+                } else if (!kv_place(p, b, kvh, wp, wrow, wslot)) {
+                    if (lane == 0) report(p.err, GEMMA_DEVERR_PAGE);
                 } else {
                     const size_t src = ((size_t)b * p.n_kv + kvh) * (size_t)D;
-                    const int slot = p.ring ? wp % p.ring : wp;
                     const size_t dst =
-                        (((size_t)b * p.n_kv + kvh) * (size_t)p.cap + slot) * (size_t)D;
+                        ((size_t)wrow * (size_t)kv_row_slots(p) + wslot) * (size_t)D;
                     for (int c = lane; c < D / 8; c += 32) {
                         const uint4 kv4 = __ldg(reinterpret_cast<const uint4*>(
                             reinterpret_cast<const __nv_bfloat16*>(p.k_new) + src) + c);
@@ -210,14 +212,17 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
             __syncwarp();
         }
         if (lane == 0) {
-            const int row3 = b * p.n_kv + kvh;
             for (int t = 0; t < n_tiles; ++t) {
                 const int s = t % S;
                 if (t >= S && !mbar_wait(&empty[s], ((t / S) - 1) & 1, p.err)) break;
                 uint8_t* dk = ring + s * stage_bytes;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
-                const int key0 = kb + t * T;
-                const int slot0 = p.ring ? key0 % p.ring : key0;  // cache slot of the tile's first key
+                // cache row and slot of the tile's first key (a bad page index reads zeros)
+                int row3 = 0, slot0 = 0;
+                if (!kv_place(p, b, kvh, kb + t * T, row3, slot0)) {
+                    report(p.err, GEMMA_DEVERR_PAGE);
+                    row3 = p.n_pages * p.n_kv;
+                }
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     tma_load_3d(dk + c * Lay::BOX, &kmap, c * 64, slot0, row3, &full[s]);
@@ -272,6 +277,9 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
         const uint8_t* tK = ring + s * stage_bytes;
         const uint8_t* tV = nops == 2 ? tK + Lay::TILE : tK;
         const int rows_valid = min(T, n_keys - t * T);
+        // a tile-aligned chunk (ring cache, paged pool) may start before every row's window:
+        // those leading keys are masked, and their values zeroed like the rows past the end
+        const int rows_head = max(0, first.lo - (kb + t * T));
 
         // (1) partial S over this warp's head_dim part
         {
@@ -349,10 +357,11 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
                 // keys of this thread's B fragment halves: k0, k0+1 (low) and k0+8, k0+9 (high)
                 const int k0 = kk * 16 + 2 * tq;
                 uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                if (rows_valid < T) {  // rows past the tile's end were not loaded: zero them
-                    mlo = (k0 < rows_valid ? 0x0000ffffu : 0u) | (k0 + 1 < rows_valid ? 0xffff0000u : 0u);
-                    mhi = (k0 + 8 < rows_valid ? 0x0000ffffu : 0u) |
-                          (k0 + 9 < rows_valid ? 0xffff0000u : 0u);
+                if (rows_valid < T || rows_head > 0) {
+                    // rows past the tile's end (not loaded) or before every window: zero them
+                    auto in = [&](int k) { return k >= rows_head && k < rows_valid; };
+                    mlo = (in(k0) ? 0x0000ffffu : 0u) | (in(k0 + 1) ? 0xffff0000u : 0u);
+                    mhi = (in(k0 + 8) ? 0x0000ffffu : 0u) | (in(k0 + 9) ? 0xffff0000u : 0u);
                 }
                 const int vkey = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
@@ -453,15 +462,15 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
     const int pos = len - n_real + token;
     const int lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
     // chunks as in the bf16 kernel (a ring cache's start at multiples of the key tile)
-    const int kb = (p.ring ? (lo & ~(kKeyTile - 1)) : lo) + split * p.chunk;
+    const int kb = ((p.ring || p.page_size) ? (lo & ~(kKeyTile - 1)) : lo) + split * p.chunk;
     const int ke = min(pos + 1, kb + p.chunk);
     if (kb >= ke) return;
 
     const float* q = reinterpret_cast<const float*>(p.q) +
                      (((size_t)b * p.n_tok + token) * p.n_q + head) * (size_t)D;
-    const size_t hb = ((size_t)b * p.n_kv + kvh) * (size_t)p.cap;
-    const float* K = reinterpret_cast<const float*>(p.k) + hb * D;
-    const float* V = reinterpret_cast<const float*>(p.v) + hb * D;
+    const float* K = reinterpret_cast<const float*>(p.k);
+    const float* V = reinterpret_cast<const float*>(p.v);
+    const size_t rs = (size_t)kv_row_slots(p);
     float qr[E], acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -470,7 +479,12 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
     }
     float m = -INFINITY, l = 0.f;
     for (int j = max(kb, lo); j < ke; ++j) {
-        const size_t row = (size_t)(p.ring ? j % p.ring : j);  // cache slot of key j
+        int krow = 0, kslot = 0;
+        if (!kv_place(p, b, kvh, j, krow, kslot)) {  // a bad page index: the key is skipped
+            if (lane == 0) report(p.err, GEMMA_DEVERR_PAGE);
+            continue;
+        }
+        const size_t row = (size_t)krow * rs + (size_t)kslot;  // cache row of key j
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) dot = fmaf(qr[e], K[row * D + lane + 32 * e], dot);
@@ -524,7 +538,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const RowsPara
         return;
     }
     int lo = p.is_sliding ? max(0, len - p.window) : 0;
-    if (p.ring) lo &= ~(kKeyTile - 1);  // chunks of a ring cache start at a tile boundary
+    if (p.ring || p.page_size) lo &= ~(kKeyTile - 1);  // chunks start at a tile boundary there
     const int nc = min(p.n_split, (len - lo + p.chunk - 1) / p.chunk);
     const size_t base = ((size_t)b * p.n_q + head) * p.n_split;
     if (tid < 32) {
@@ -620,8 +634,11 @@ static cudaError_t launch_bf16_d(const RowsParams& p, dim3 grid, size_t smem, cu
         configured = true;
     }
     CUtensorMap km, vm;
-    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.cap, (uint64_t)grid.z * p.n_kv};
-    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.cap * D * 2};
+    // [rows][slots][D]: rows = sequences x KV heads (pages x KV heads for a paged pool)
+    const uint64_t map_slots = p.page_size ? (uint64_t)p.page_size : (uint64_t)p.cap;
+    const uint64_t map_rows = p.page_size ? (uint64_t)p.n_pages * p.n_kv : (uint64_t)grid.z * p.n_kv;
+    const uint64_t dims[3] = {(uint64_t)D, map_slots, map_rows};
+    const uint64_t strides[2] = {(uint64_t)D * 2, map_slots * D * 2};
     const uint32_t box[3] = {64, (uint32_t)kKeyTile, 1};
     if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;

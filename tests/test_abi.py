@@ -170,3 +170,29 @@ def test_logit_argument_errors(args, status):
     assert lib().gemma_logit_workspace_size(-1, 4) == ctypes.c_size_t(-1).value
     assert lib().gemma_logit_workspace_size(1, 0) == ctypes.c_size_t(-1).value
     assert lib().gemma_logit_workspace_size(0, 4) == 0
+
+
+def test_paged_argument_checks():
+    """The paged entry points reject a page size that is not a multiple of 128, empty pools and
+    ring kinds on the host."""
+    f = lib().gemma_attn_paged
+    base = dict(max_pages=4, page_size=128, n_pages=8, kind=1, msl=64)
+
+    def call(**kw):
+        a = {**base, **kw}
+        return f(FAKE, FAKE, _ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, FAKE, a["max_pages"],
+                 a["page_size"], a["n_pages"], a["msl"], 1, 1, a["kind"], 0, 4, 1, 64, 1, 0.125,
+                 0, None, None, None, None, 0, None, None)
+    assert call(page_size=100) == UNSUPPORTED
+    assert call(page_size=64) == UNSUPPORTED
+    assert call(n_pages=0) == INVALID
+    assert call(max_pages=0) == INVALID
+    assert call(kind=2) == INVALID
+    assert call(msl=513) == CAPACITY   # beyond max_pages * page_size
+    a = lib().gemma_kv_append_paged
+    assert a(_ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, None, FAKE, None, 4, 128, 8, 1, 1,
+             1, 64, 1, 0, None, None) == INVALID   # block table missing
+    assert a(_ptrs(FAKE), _ptrs(None), _i32(0), 1, 0, FAKE, None, FAKE, FAKE, 4, 130, 8, 1, 1,
+             1, 64, 1, 0, None, None) == UNSUPPORTED
+    assert lib().gemma_attn_workspace_size_paged(1, 2, 512, 4, 1, 64, 64, 1) == \
+        ctypes.c_size_t(-1).value
