@@ -40,13 +40,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 RAGGED_PHYS_LAYERS = 6   # distinct caches for 48 ragged layer-steps (one 5:1 period)
 SOFTCAP_EXAMPLE = 50.0   # attention-logit soft-cap used to time the soft-capped entry point
 BUCKET_REAL_EXAMPLE = [512, 384, 256, 128]   # real rows per sequence of the padded bucket timed
-RING_EXAMPLE = 1024      # ring slots of the sliding layers' caches (the 12B window)
+RING_EXAMPLE = 1024     # ring slots of the sliding layers' caches (the 12B window)
+PAGE_EXAMPLE = 256      # keys per page of the paged pools
 
 # dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
 # captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
 # batch-64 global layer); used only while the kernel sources hash to the recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": "663378c2339e20eff5155d53031455c4c073a056",
-                      "per_algorithmic_byte": {"sliding": 1.0229, "global": 1.0349}}
+NCU_DECODE_TRAFFIC = {"source_sha1": "e46d9f8b5dc9ae149886bb8a20e57ec33969bfd6",
+                      "per_algorithmic_byte": {"sliding": 1.0225, "global": 1.0335}}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -156,12 +157,17 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------------
 class DeviceState:
     def __init__(self, w, seed, device, phys_of_layer=None, softcap=None, n_real=None,
-                 fused=False, ring=None):
+                 fused=False, ring=None, paged=None):
         import mixed_sliding_global_gb300 as g
         self.g, self.w, self.device = g, w, device
         self.softcap = softcap
         self.fused = fused  # decode: append inside the attention launch (one launch per layer)
         self.ring = ring    # sliding layers' caches: rings of this many slots (None: linear)
+        # paged pools with pages of this many keys (None: one linear cache per sequence): a
+        # global layer's pool holds the pages of positions [0, len), a sliding layer's only the
+        # pages from its window start; pages are handed out in a seeded shuffled order
+        self.paged = paged
+        self.tables = {}
         # padded prefill bucket: real rows per sequence (the rest pad the bucket to n_new)
         self.n_real = None if n_real is None else torch.tensor(n_real, dtype=torch.int32,
                                                                 device=device)
@@ -182,7 +188,9 @@ class DeviceState:
             if w.is_owner(l):
                 p = phys[l]
                 if p not in kc_phys:
-                    if ring and s.kind == synth.SLIDING:
+                    if paged:
+                        kc_phys[p], vc_phys[p] = self._pools(s, B, dt)
+                    elif ring and s.kind == synth.SLIDING:
                         # a ring holds the last `ring` tokens: every slot is a real past token
                         kc_phys[p] = self._randn((B, s.n_kv, ring, s.head_dim), dt)
                         vc_phys[p] = None if s.k_eq_v else self._randn((B, s.n_kv, ring, s.head_dim), dt)
@@ -196,8 +204,9 @@ class DeviceState:
             self.q[l] = self._randn((B, w.n_new, s.n_q, s.head_dim), dt)
             self.out[l] = torch.empty_like(self.q[l])
         msl = max(w.ctx_lens)
-        ws = max(g.gemma_attn_workspace_size(B, self.kind_of(s), s.window, s.n_q, s.n_kv,
-                                             s.head_dim, msl, w.n_new) for s in w.layers)
+        wsf = g.gemma_attn_workspace_size_paged if paged else g.gemma_attn_workspace_size
+        ws = max(wsf(B, self.kind_of(s), s.window, s.n_q, s.n_kv, s.head_dim, msl, w.n_new)
+                 for s in w.layers)
         self.ws = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
         self.max_seq_len = msl
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -215,6 +224,30 @@ class DeviceState:
             lo = synth.needed_row_lo(s, ctx, self.w.n_new)
             c[b, :, lo:ctx].copy_(self._randn((s.n_kv, ctx - lo, s.head_dim), dt))
         return c
+
+    def _pools(self, s, B, dt):
+        """K (and V) pools of one owner layer and the block table of its kind."""
+        P, w = self.paged, self.w
+        max_pages = -(-w.capacity // P)
+        if s.kind not in self.tables:
+            first = []
+            for ctx in w.ctx_lens:
+                lo = 0 if s.kind == synth.GLOBAL else max(0, ctx - s.window) & ~31
+                first.append(lo // P)
+            need = [-(-ctx // P) - f for ctx, f in zip(w.ctx_lens, first)]
+            n_pages = sum(need)
+            g = torch.Generator().manual_seed(4242 + s.kind)
+            perm = torch.randperm(n_pages, generator=g)
+            table = torch.zeros((B, max_pages), dtype=torch.int32)   # unread entries: page 0
+            k = 0
+            for b in range(B):
+                table[b, first[b]:first[b] + need[b]] = perm[k:k + need[b]].to(torch.int32)
+                k += need[b]
+            self.tables[s.kind] = (table.to(self.device), n_pages)
+        n_pages = self.tables[s.kind][1]
+        kp = self._randn((n_pages, s.n_kv, P, s.head_dim), dt)
+        vp = None if s.k_eq_v else self._randn((n_pages, s.n_kv, P, s.head_dim), dt)
+        return kp, vp
 
     def kind_of(self, s):
         return self.g.GEMMA_SLIDING_RING if self.ring and s.kind == synth.SLIDING else s.kind
@@ -255,6 +288,14 @@ class DeviceState:
     def fused_call(self, l):
         w, s = self.w, self.w.layers[l]
         o = w.owner_map[l]
+        if self.paged:
+            self.g.gemma_attn_paged(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l,
+                                    self.seq_lens, self.tables[s.kind][0], self.max_seq_len,
+                                    kind=s.kind, window=s.window, n_kv=s.n_kv, k_eq_v=s.k_eq_v,
+                                    scale=w.scale(l), k_new=self.k_new[o], v_new=self.v_new[o],
+                                    write_pos=self.write_pos, workspace=self.ws,
+                                    device_error=self.err)
+            return
         self.g.gemma_attn_decode_append(self.out[l], self.q[l], self.kc, self.vc, w.owner_map, l,
                                         self.k_new[o], self.v_new[o], self.write_pos,
                                         self.seq_lens, self.max_seq_len, kind=self.kind_of(s),
@@ -285,8 +326,10 @@ class DeviceState:
         for l, s in enumerate(w.layers):
             n += 1 if w.is_owner(l) and not self.fused else 0
             n += 1
-            if w.n_new == 1 and self.g.gemma_attn_workspace_size(
-                    w.batch, s.kind, s.window, s.n_q, s.n_kv, s.head_dim, self.max_seq_len, 1) > 0:
+            wsf = self.g.gemma_attn_workspace_size_paged if self.paged else \
+                self.g.gemma_attn_workspace_size
+            if w.n_new == 1 and wsf(w.batch, s.kind, s.window, s.n_q, s.n_kv, s.head_dim,
+                                    self.max_seq_len, 1) > 0:
                 n += 1  # split combine
         return n
 
@@ -378,11 +421,11 @@ def workload(name, batch=None, layers=None, offset=0):
 
 
 def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rotations=1,
-                    softcap=None, n_real=None, fused=False, ring=None):
+                    softcap=None, n_real=None, fused=False, ring=None, paged=None):
     """Capture one graph per step (rotating over `rotations` independent input copies) and
     time `steps` replays after `warmup` replays. Returns step time and, with per_launch, the
     mean duration of each layer's attention launch over the timed replays."""
-    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap, n_real, fused, ring)
+    states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap, n_real, fused, ring, paged)
               for r in range(rotations)]
     for st in states:   # eager pass: sets kernel attributes, checks the error word
         st.step()
@@ -670,20 +713,25 @@ def run_native(args):
         # plain rows append inside the attention launch)
         # ragged_decode_ring: the headline workload with its sliding layers' caches as rings of
         # 1024 slots (the window) instead of 16448 rows
+        # ragged_decode_paged: the headline workload over paged pools of 256-key pages holding
+        # only the pages the step reads (global: [0, len); sliding: from the window start)
         for name in [n for n in ("prefill", "prefill_softcap", "prefill_bucket", "12b_decode",
                                  "12b_decode_two_launch", "e4b_decode", "e4b_decode_two_launch",
-                                 "ragged_decode_ring") if n != args.workload]:
+                                 "ragged_decode_ring", "ragged_decode_paged")
+                     if n != args.workload]:
             cap2 = SOFTCAP_EXAMPLE if name == "prefill_softcap" else None
             real2 = BUCKET_REAL_EXAMPLE if name == "prefill_bucket" else None
             fused2 = not name.startswith("prefill") and not name.endswith("_two_launch")
             ring2 = RING_EXAMPLE if name == "ragged_decode_ring" else None
+            paged2 = PAGE_EXAMPLE if name == "ragged_decode_paged" else None
             w2, phys2 = workload("prefill" if name.startswith("prefill") else
-                                 name.replace("_two_launch", "").replace("_ring", ""))
+                                 name.replace("_two_launch", "").replace("_ring", "")
+                                 .replace("_paged", ""))
             rot = 12 if name.startswith("e4b_decode") else 1   # e4b inputs rotate past L2
             ms2, lm2, clk2, info2 = timed_graph_run(w2, phys2, args.steps, args.warmup, device,
                                                     world, per_launch=(w2.n_new > 1),
                                                     rotations=rot, softcap=cap2, n_real=real2,
-                                                    fused=fused2, ring=ring2)
+                                                    fused=fused2, ring=ring2, paged=paged2)
             ms2 = max_over_ranks(ms2, world)
             d2 = w2.n_new == 1
             u2, sc2 = ("GB/s", 1e9) if d2 else ("TFLOP/s", 1e12)
@@ -714,6 +762,9 @@ def run_native(args):
                 ent["n_real"] = real2
             if ring2 is not None:
                 ent["ring_slots"] = ring2
+                ent["cache_gb"] = info2["cache_bytes"] / 1e9
+            if paged2 is not None:
+                ent["page_size"] = paged2
                 ent["cache_gb"] = info2["cache_bytes"] / 1e9
             also[name] = ent
         # the greedy step after the LM head: final-logit soft-cap 30 (capped logits written)
