@@ -46,8 +46,8 @@ PAGE_EXAMPLE = 256      # keys per page of the paged pools
 # dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
 # captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
 # batch-64 global layer); used only while the kernel sources hash to the recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": "e46d9f8b5dc9ae149886bb8a20e57ec33969bfd6",
-                      "per_algorithmic_byte": {"sliding": 1.0225, "global": 1.0335}}
+NCU_DECODE_TRAFFIC = {"source_sha1": "0193662704743271364351d4d391e67b32adb15f",
+                      "per_algorithmic_byte": {"sliding": 1.0230, "global": 1.0336}}
 
 
 # ---------------------------------------------------------------------------------------------

@@ -142,6 +142,31 @@ GEMMA_DEVINL float fast_exp2(float x) {
     return y;
 }
 
+// Programmatic dependent launch: every kernel of this library lets the next kernel on its
+// stream be scheduled as soon as it starts, and waits for the previous kernel to complete (and
+// its memory to be visible) before its own first global memory access; so a kernel's launch
+// latency overlaps its predecessor's tail while the order of memory accesses stays the
+// stream's. Without the launch attribute both instructions have no effect.
+GEMMA_DEVINL void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+GEMMA_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with the programmatic-stream-serialization attribute (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 GEMMA_DEVINL uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint8_t* __restrict__ kc
                                                         int batch, int n_new, int n_kv,
                                                         int capacity, int row_bytes,
                                                         uint32_t* err) {
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel on the stream has completed
     const int chunks = row_bytes / 16;
     const long long total = (long long)batch * n_new * n_kv * chunks;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -78,11 +80,10 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k_new, co
     const long long cap_blocks = (long long)n_sm * 8;
     if (blocks > cap_blocks) blocks = cap_blocks;
     if (blocks < 1) blocks = 1;
-    kv_append_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
-        static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new), write_pos, n_real,
-        ring, pg, batch, n_new, n_kv, capacity, row_bytes, err);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
+                      static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new),
+                      write_pos, n_real, ring, pg, batch, n_new, n_kv, capacity, row_bytes, err);
 }
 
 }  // namespace gemma

@@ -123,6 +123,8 @@ struct LgTraits<float> {
 
 template <typename T, bool CAPPED>
 __global__ void __launch_bounds__(kLgThreads) logit_split_kernel(const LogitParams p) {
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel on the stream has completed
     using Tr = LgTraits<T>;
     constexpr int VEC = Tr::VEC;
     __shared__ unsigned long long s_best[kLgThreads / 32];
@@ -212,6 +214,8 @@ __global__ void __launch_bounds__(kLgThreads) logit_split_kernel(const LogitPara
 }
 
 __global__ void __launch_bounds__(32) logit_finish_kernel(const LogitParams p) {
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel on the stream has completed
     const int b = blockIdx.x, lane = threadIdx.x;
     const long long N = p.total, C = p.n_cta;
     const long long first = (long long)b * p.vocab;
@@ -271,19 +275,15 @@ cudaError_t launch_logit_softcap_argmax(const void* logits, void* capped, int32_
     p.n_cta = pl.n_cta;
     p.softcap = softcap;
     p.inv_cap = softcap > 0.f ? 1.f / softcap : 0.f;
-    const dim3 grid(pl.n_cta);
-    if (fp32) {
-        if (capped) logit_split_kernel<float, true><<<grid, kLgThreads, 0, st>>>(p);
-        else logit_split_kernel<float, false><<<grid, kLgThreads, 0, st>>>(p);
-    } else {
-        if (capped) logit_split_kernel<__nv_bfloat16, true><<<grid, kLgThreads, 0, st>>>(p);
-        else logit_split_kernel<__nv_bfloat16, false><<<grid, kLgThreads, 0, st>>>(p);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess) {
-        logit_finish_kernel<<<batch, 32, 0, st>>>(p);
-        e = cudaGetLastError();
-    }
+    const dim3 grid(pl.n_cta), block(kLgThreads);
+    cudaError_t e;
+    if (fp32)
+        e = capped ? launch_pdl(logit_split_kernel<float, true>, grid, block, 0, st, p)
+                   : launch_pdl(logit_split_kernel<float, false>, grid, block, 0, st, p);
+    else
+        e = capped ? launch_pdl(logit_split_kernel<__nv_bfloat16, true>, grid, block, 0, st, p)
+                   : launch_pdl(logit_split_kernel<__nv_bfloat16, false>, grid, block, 0, st, p);
+    if (e == cudaSuccess) e = launch_pdl(logit_finish_kernel, dim3(batch), dim3(32), 0, st, p);
     return e;
 }
 

@@ -132,6 +132,8 @@ template <int D, int CL, bool SOFTCAP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const TcParams tp) {
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel on the stream has completed
     using Lay = TcLayout<D, CL>;
     constexpr int DH = Lay::DH;
     const RowsParams& p = tp.p;
@@ -596,13 +598,15 @@ static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, true>, km, vm, tp)
                            : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, false>, km, vm, tp);
 }

@@ -94,6 +94,8 @@ template <int D>
 __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     rows_attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const RowsParams p) {
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel on the stream has completed
     using Lay = RowsLayout<D>;
     constexpr int T = kKeyTile;
     constexpr int KSPLIT = Lay::KSPLIT;
@@ -435,6 +437,8 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
 // ---------------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(const RowsParams p) {
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel on the stream has completed
     constexpr int E = D / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x % p.n_split;
@@ -526,6 +530,8 @@ constexpr int kCombineGroups = 4;
 
 template <typename OutT>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const RowsParams p, int D) {
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel on the stream has completed
     __shared__ float s_w[128];                                  // chunk weights (n_split <= 128)
     __shared__ float s_red[kCombineGroups][kCombineThreads / kCombineGroups * 4];
     __shared__ float s_inv;
@@ -642,8 +648,7 @@ static cudaError_t launch_bf16_d(const RowsParams& p, dim3 grid, size_t smem, cu
     const uint32_t box[3] = {64, (uint32_t)kKeyTile, 1};
     if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    rows_attn_bf16_kernel<D><<<grid, kRowsThreads, smem, st>>>(km, vm, p);
-    return cudaGetLastError();
+    return launch_pdl(rows_attn_bf16_kernel<D>, grid, dim3(kRowsThreads), smem, st, km, vm, p);
 }
 
 cudaError_t launch_rows_bf16(const RowsParams& p, int head_dim, dim3 grid, size_t smem,
@@ -660,24 +665,20 @@ cudaError_t launch_rows_bf16(const RowsParams& p, int head_dim, dim3 grid, size_
 cudaError_t launch_rows_f32(const RowsParams& p, int head_dim, dim3 grid, cudaStream_t st) {
     const dim3 block(kF32RowsPerCta * 32);
     switch (head_dim) {
-        case 64: rows_attn_f32_kernel<64><<<grid, block, 0, st>>>(p); break;
-        case 128: rows_attn_f32_kernel<128><<<grid, block, 0, st>>>(p); break;
-        case 256: rows_attn_f32_kernel<256><<<grid, block, 0, st>>>(p); break;
-        case 512: rows_attn_f32_kernel<512><<<grid, block, 0, st>>>(p); break;
+        case 64: return launch_pdl(rows_attn_f32_kernel<64>, grid, block, 0, st, p);
+        case 128: return launch_pdl(rows_attn_f32_kernel<128>, grid, block, 0, st, p);
+        case 256: return launch_pdl(rows_attn_f32_kernel<256>, grid, block, 0, st, p);
+        case 512: return launch_pdl(rows_attn_f32_kernel<512>, grid, block, 0, st, p);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out_fp32,
                            cudaStream_t st) {
     const dim3 grid(p.n_q, batch);
     const dim3 block(kCombineThreads);
-    if (out_fp32)
-        combine_kernel<float><<<grid, block, 0, st>>>(p, head_dim);
-    else
-        combine_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(p, head_dim);
-    return cudaGetLastError();
+    if (out_fp32) return launch_pdl(combine_kernel<float>, grid, block, 0, st, p, head_dim);
+    return launch_pdl(combine_kernel<__nv_bfloat16>, grid, block, 0, st, p, head_dim);
 }
 
 }  // namespace gemma
