@@ -2,9 +2,10 @@
 
 The greedy index is compared exactly (it is decided on the raw logits by exact comparisons on
 both sides). The capped logits are compared within a relative bound derived from the
-arithmetic: the kernel's tanh approximation (relative error below 2^-10.9) plus one rounding to
-the output dtype (2^-9 relative for bf16, 2^-24 for fp32) and fp32 multiplies, so
-|got - ref| <= 2^-8 |ref| for bf16 and 2^-10 |ref| for fp32 output, plus 1e-6 absolute."""
+arithmetic: the kernel's tanh approximation (relative error below 2^-10.9 away from zero, a
+small absolute floor near zero) plus one rounding to the output dtype (2^-9 relative for bf16,
+2^-24 for fp32) and fp32 multiplies, so |got - ref| <= 2^-8 |ref| for bf16 and 2^-10 |ref| for
+fp32 output, plus 1e-6 absolute for the logits nearest zero."""
 import pytest
 import torch
 
