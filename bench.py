@@ -44,10 +44,11 @@ RING_EXAMPLE = 1024     # ring slots of the sliding layers' caches (the 12B wind
 PAGE_EXAMPLE = 256      # keys per page of the paged pools
 
 # dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
-# captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-16 sliding layer and a
-# batch-64 global layer); used only while the kernel sources hash to the recorded value
+# captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-40 sliding layer in the
+# unsplit launch configuration of the batch-64 one, and a batch-64 global layer); used only
+# while the kernel sources hash to the recorded value
 NCU_DECODE_TRAFFIC = {"source_sha1": "0193662704743271364351d4d391e67b32adb15f",
-                      "per_algorithmic_byte": {"sliding": 1.0230, "global": 1.0336}}
+                      "per_algorithmic_byte": {"sliding": 1.0155, "global": 1.0336}}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -400,10 +401,14 @@ def _slice(w, offset, nl):
                           w.n_new, w.ctx_lens, w.capacity)
 
 
-def workload(name, batch=None, layers=None, offset=0):
+def workload(name, batch=None, layers=None, offset=0, max_len=None):
     if name == "ragged_decode":
         nl = layers or 48
-        w = synth.ragged_decode(n_layers=offset + nl, batch=batch or 64)
+        if max_len:   # shorter sequences and a smaller cache (profiling captures only)
+            w = synth.ragged_decode(n_layers=offset + nl, batch=batch or 64,
+                                    capacity=-(-(max_len + 1) // 64) * 64, max_len=max_len)
+        else:
+            w = synth.ragged_decode(n_layers=offset + nl, batch=batch or 64)
         if offset:
             w = _slice(w, offset, nl)
         return w, [(offset + l) % RAGGED_PHYS_LAYERS for l in range(nl)]
@@ -621,7 +626,7 @@ def run_native(args):
     build_library(world, local)
     device = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    w, phys = workload(args.workload, args.batch, args.layers, args.layer_offset)
+    w, phys = workload(args.workload, args.batch, args.layers, args.layer_offset, args.max_len)
     decode = w.n_new == 1
     unit = "GB/s" if decode else "TFLOP/s"
     scale = 1e9 if decode else 1e12
@@ -650,9 +655,15 @@ def run_native(args):
         traffic = None
         if NCU_DECODE_TRAFFIC["source_sha1"] == kernel_source_sha1():
             traffic = NCU_DECODE_TRAFFIC["per_algorithmic_byte"][dom] * b / n
+        import mixed_sliding_global_gb300 as gemma
+        sd = next(s for s in w.layers if (s.kind == synth.SLIDING) == (dom == "sliding"))
+        split = gemma.gemma_attn_workspace_size(w.batch, sd.kind, sd.window, sd.n_q, sd.n_kv,
+                                                sd.head_dim, max(w.ctx_lens), 1) > 0
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": f"rows_attn_bf16_kernel<{d}> + split combine ({dom} layers)",
+                "kernel": f"rows_attn_bf16_kernel<{d}>" +
+                          (" + split combine" if split else " (one CTA per sequence and KV head)") +
+                          f" ({dom} layers)",
                 "algorithmic_bytes_per_launch": b / n, "launch_us": 1e3 * t / n,
                 "peak_source": peak_src}
         for name, (bk, tk, nk, dk) in kinds.items():
@@ -680,8 +691,9 @@ def run_native(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) drawn on the device, stored as bf16)",
             "config": {"workload": args.workload, "batch": w.batch, "layers": w.n_layers,
-                       "n_new": w.n_new, "ctx": ("uniform[129,16385]" if args.workload ==
-                                                 "ragged_decode" else max(w.ctx_lens)),
+                       "n_new": w.n_new, "ctx": (f"uniform[129,{16384 if not args.max_len else args.max_len}+1]"
+                                                 if args.workload == "ragged_decode"
+                                                 else max(w.ctx_lens)),
                        "parallelism": f"dp{world}" if world > 1 else "single",
                        "l2": "inputs larger than L2 (each layer-step reads > 129 MB)"
                        if args.workload == "ragged_decode" else "inputs larger than L2",
@@ -798,6 +810,8 @@ def main():
                     help="smaller ragged batch (profiling captures only; not a bench line)")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer ragged layer-steps (profiling captures only; not a bench line)")
+    ap.add_argument("--max-len", type=int, default=None,
+                    help="ragged lengths up to this (profiling captures only; not a bench line)")
     ap.add_argument("--layer-offset", type=int, default=0,
                     help="first ragged layer (profiling captures only; not a bench line)")
     ap.add_argument("--two-launch", action="store_true",

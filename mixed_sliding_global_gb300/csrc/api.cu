@@ -20,6 +20,10 @@ constexpr int kMaxSplit = 128;
 #define GEMMA_SPLIT_CTAS_PER_SM 8
 #endif
 constexpr int kMinChunkKeys = GEMMA_MIN_CHUNK_KEYS;  // keys per split chunk when work is plentiful
+// no split when the (sequence, KV head) units alone fill the GPU (at least this many per SM)
+// and each attends a short key range: one CTA per unit, no partials, no combine launch
+constexpr long long kNoSplitUnitsPerSm = 2;
+constexpr long long kNoSplitMaxKeys = 2048;
 constexpr long long kSplitCtasPerSm = GEMMA_SPLIT_CTAS_PER_SM;
 
 int sm_count() {
@@ -68,7 +72,8 @@ struct Plan {
 
 // Decode splits each (sequence, KV head) key range into chunks so that enough CTAs stream
 // the cache at once: about one chunk per SM for small problems, about eight per SM (and at
-// least kMinChunkKeys keys each) for large ones. Prefill has one row tile per 16 rows and no
+// least kMinChunkKeys keys each) for large ones; not at all when the units alone fill the GPU
+// over short key ranges (a sliding window across a large batch). Prefill has one row tile per 16 rows and no
 // split. Depends only on the arguments and the SM count.
 Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim, int max_seq_len,
                int n_tok, int n_sm, bool paged = false) {
@@ -79,6 +84,7 @@ Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim,
     // a ring cache's or paged pool's key tiles start at multiples of the tile (so that none wraps
     // or crosses a page): up to T - 1 keys before the window join the range
     if (kind == GEMMA_SLIDING_RING || paged) n_read += T - 1;
+    if ((long long)batch * n_kv >= kNoSplitUnitsPerSm * n_sm && n_read <= kNoSplitMaxKeys) return pl;
     const long long total = (long long)batch * n_kv * n_read;
     const long long one_per_sm = round_up((total + n_sm - 1) / n_sm, T);
     const long long eight_per_sm =

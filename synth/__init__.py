@@ -119,10 +119,11 @@ def ragged_lengths(batch: int = 64, lo: int = 128, hi: int = 16384) -> List[int]
     return torch.randint(lo, hi + 1, (batch,), generator=g).tolist()
 
 
-def ragged_decode(n_layers: int = 48, batch: int = 64, capacity: int = 16448) -> Workload:
+def ragged_decode(n_layers: int = 48, batch: int = 64, capacity: int = 16448,
+                  max_len: int = 16384) -> Workload:
     """Batched ragged decode on 12B-shaped layers: one new token per sequence is
-    appended at slot L_b, attention length L_b + 1."""
-    pre = ragged_lengths(batch)
+    appended at slot L_b, attention length L_b + 1 (L_b uniform in [128, max_len])."""
+    pre = ragged_lengths(batch, hi=max_len)
     return Workload("ragged_decode", _layers_12b(n_layers), list(range(n_layers)), batch, BF16, 1,
                     [p + 1 for p in pre], capacity)
 

@@ -200,3 +200,22 @@ def test_workspace_is_reusable_across_calls():
             torch.cuda.synchronize()
             assert gr.err.item() == 0
             assert torch.equal(out, fresh), (rep, spec)
+
+
+def test_ragged_decode_full_batch_sliding_layer():
+    """The batch-64 ragged decode's sliding layer in the launch configuration the benchmark
+    times (512 (sequence, KV head) units fill the GPU: one CTA each, no split), checked on
+    sampled sequences; their seeded inputs equal those of the full batch."""
+    w = synth.ragged_decode(n_layers=6)
+    lens = w.ctx_lens
+    seqs = sorted({lens.index(min(lens)), lens.index(max(lens)), 7, 33, 63})
+    hb = host_inputs(w, [0])
+    gr = GpuRun(w, hb)
+    gr.append(0)
+    got = gr.attend(0, max_seq_len=max(lens))
+    torch.cuda.synchronize()
+    assert gr.err.item() == 0
+    sub = Workload(w.name, w.layers, w.owner_map, len(seqs), w.dtype, 1, [lens[s] for s in seqs],
+                   w.capacity)
+    ref = oracle_outputs(sub, host_inputs(w, [0], seqs), [0])[0]
+    compare(got[seqs].cpu(), ref, w.dtype)
