@@ -314,8 +314,8 @@ size_t gemma_attn_workspace_size_paged(int batch, gemma_layer_kind kind, int win
  * softcap); the argmax of the capped logits is the argmax of the raw ones, so greedy decoding
  * does not depend on the cap). The index is therefore taken on the raw logits: an exact
  * comparison, the same in every precision. NaN entries are never selected; a row of NaN gives
- * index 0. tanh is evaluated with the hardware approximation (relative error below 2^-10 away
- * from zero, a small absolute error near zero).
+ * index 0. For bf16 logits tanh is the hardware approximation (relative error below 2^-10.9,
+ * a fraction of the bf16 rounding); for fp32 logits the accurate library tanhf.
  *   logits      DEVICE [batch][vocab] of dtype, row-major, 16-byte aligned (caller-owned).
  *   capped_out  DEVICE [batch][vocab] of dtype, 16-byte aligned, or NULL to skip the capped
  *               logits; may equal logits (in place).

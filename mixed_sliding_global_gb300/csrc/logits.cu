@@ -63,12 +63,15 @@ GEMMA_DEVINL long long cta_begin(long long c, long long N, long long C) { return
 GEMMA_DEVINL long long cta_of(long long e, long long N, long long C) { return e * C / N; }
 
 // Per-vector operations on one 16-byte vector of logits: its maximum (NaN ignored unless all
-// are NaN), element e, and the capped vector c * tanh(x / c).
+// are NaN), element e, and the capped vector c * tanh(x / c). tanh: the hardware approximation
+// for bf16 output (its relative error, below 2^-10.9, is a fraction of the bf16 rounding,
+// 2^-8), the accurate library function for fp32 output.
 template <typename T>
 struct LgTraits;
 template <>
 struct LgTraits<__nv_bfloat16> {
     static constexpr int VEC = 8;
+    GEMMA_DEVINL static float tanh1(float x) { return tanh_approx(x); }
     GEMMA_DEVINL static float vmax(const uint4& v) {
         uint32_t m;
         asm("{\n\t.reg .b32 t0, t1;\n\t"
@@ -85,8 +88,8 @@ struct LgTraits<__nv_bfloat16> {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const uint32_t w = (&v.x)[k];
-            const float y0 = c * tanh_approx(__uint_as_float(w << 16) * ic);
-            const float y1 = c * tanh_approx(__uint_as_float(w & 0xffff0000u) * ic);
+            const float y0 = c * tanh1(__uint_as_float(w << 16) * ic);
+            const float y1 = c * tanh1(__uint_as_float(w & 0xffff0000u) * ic);
             (&o.x)[k] = pack_bf16(y0, y1);
         }
         return o;
@@ -101,6 +104,7 @@ struct LgTraits<__nv_bfloat16> {
 template <>
 struct LgTraits<float> {
     static constexpr int VEC = 4;
+    GEMMA_DEVINL static float tanh1(float x) { return tanhf(x); }
     GEMMA_DEVINL static float vmax(const uint4& v) {
         return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
                      fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
@@ -110,7 +114,7 @@ struct LgTraits<float> {
         uint4 o;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            (&o.x)[k] = __float_as_uint(c * tanh_approx(__uint_as_float((&v.x)[k]) * ic));
+            (&o.x)[k] = __float_as_uint(c * tanh1(__uint_as_float((&v.x)[k]) * ic));
         return o;
     }
     GEMMA_DEVINL static float load1(const void* p, size_t i) {
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(kLgThreads) logit_split_kernel(const LogitPara
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long N = p.total, C = p.n_cta, c = blockIdx.x;
     const long long e_end = cta_begin(c + 1, N, C);
-    auto cap = [&](float x) { return p.softcap > 0.f ? p.softcap * tanh_approx(x * p.inv_cap) : x; };
+    auto cap = [&](float x) { return p.softcap > 0.f ? p.softcap * Tr::tanh1(x * p.inv_cap) : x; };
     for (long long e = cta_begin(c, N, C); e < e_end;) {  // one pass per row the range touches
         const int b = (int)(e / p.vocab);
         const long long row = (long long)b * p.vocab;

@@ -2,10 +2,10 @@
 
 The greedy index is compared exactly (it is decided on the raw logits by exact comparisons on
 both sides). The capped logits are compared within a relative bound derived from the
-arithmetic: the kernel's tanh approximation (relative error below 2^-10.9 away from zero, a
-small absolute floor near zero) plus one rounding to the output dtype (2^-9 relative for bf16,
-2^-24 for fp32) and fp32 multiplies, so |got - ref| <= 2^-8 |ref| for bf16 and 2^-10 |ref| for
-fp32 output, plus 1e-6 absolute for the logits nearest zero."""
+arithmetic: bf16 output is one rounding to 8 significant bits (2^-8 relative) after the hardware
+tanh approximation (relative error below 2^-10.9) and fp32 multiplies, so |got - ref| <=
+(2^-8 + 2^-10) |ref|; fp32 output uses the library tanhf (a few ulp) and fp32 multiplies, so
+|got - ref| <= 2^-20 |ref|; both plus 1e-6 absolute for the logits nearest zero."""
 import pytest
 import torch
 
@@ -14,7 +14,7 @@ import synth
 
 pytestmark = pytest.mark.gpu
 
-REL = {synth.BF16: 2.0 ** -8, synth.FP32: 2.0 ** -10}
+REL = {synth.BF16: 2.0 ** -8 + 2.0 ** -10, synth.FP32: 2.0 ** -20}
 
 
 def run(x_host, softcap, capped=True, in_place=False):
