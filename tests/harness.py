@@ -59,7 +59,7 @@ def oracle_outputs(w: synth.Workload, hb: Dict[int, synth.LayerBatch], layers: S
     return out
 
 
-class GpuRun:
+class DeviceRun:
     """Device copies of a workload's host inputs and the C-ABI calls of one step."""
 
     def __init__(self, w: synth.Workload, hb: Dict[int, synth.LayerBatch], device="cuda"):

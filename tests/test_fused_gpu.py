@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import mixed_sliding_global_gb300 as g
-from harness import GpuRun, compare, host_inputs, oracle_outputs
+from harness import DeviceRun, compare, host_inputs, oracle_outputs
 from synth import BF16, FP32, GLOBAL, SLIDING, LayerSpec, Workload
 
 pytestmark = pytest.mark.gpu
@@ -50,11 +50,11 @@ SHAPES = [
 def test_fused_equals_append_then_decode(spec, ctx, cap, dtype):
     w = one_layer(spec, ctx, cap, dtype)
     hb = host_inputs(w, [0])
-    two = GpuRun(w, hb)
+    two = DeviceRun(w, hb)
     two.append(0)
     ref = two.attend(0)
     torch.cuda.synchronize()
-    one = GpuRun(w, hb)
+    one = DeviceRun(w, hb)
     got = fused(one, w)
     assert one.err.item() == 0 and two.err.item() == 0
     assert torch.equal(got, ref)
@@ -72,7 +72,7 @@ def test_fused_slot_before_the_last_position_and_outside_the_window():
     hb = host_inputs(w, [0])
     for wp in ([2995, 100], [2999, 2990]):
         pos = torch.tensor(wp, dtype=torch.int32)
-        two, one = GpuRun(w, hb), GpuRun(w, hb)
+        two, one = DeviceRun(w, hb), DeviceRun(w, hb)
         for gr in (two, one):   # the last slot holds finite data when the new row goes elsewhere
             gr.kc[0][:, :, 2999] = 0.25
             gr.vc[0][:, :, 2999] = -0.5
@@ -91,7 +91,7 @@ def test_fused_on_a_shared_layer_is_plain_decode():
     layers = [LayerSpec(GLOBAL, 0, 8, 2, 256, False)] * 2
     w = Workload("fused_shared", layers, [0, 0], 2, BF16, 1, [900, 2000], 2048)
     hb = host_inputs(w, [0, 1])
-    gr = GpuRun(w, hb)
+    gr = DeviceRun(w, hb)
     gr.append(0)
     ref = gr.attend(1)
     before = gr.kc[0].clone()
@@ -104,7 +104,7 @@ def test_fused_write_pos_out_of_range_is_reported():
     spec = LayerSpec(GLOBAL, 0, 4, 1, 64, True)
     w = one_layer(spec, [60, 60], 64)
     hb = host_inputs(w, [0])
-    gr = GpuRun(w, hb)
+    gr = DeviceRun(w, hb)
     before = gr.kc[0].clone()
     fused(gr, w, write_pos=torch.tensor([64, 59], dtype=torch.int32, device="cuda"))
     assert gr.err.item() & g.GEMMA_DEVERR_WRITE_POS

@@ -5,7 +5,7 @@ must place the new rows exactly where the plain append does (gathered back, bit 
 import pytest
 import torch
 
-from harness import GpuRun, compare, host_inputs, oracle_outputs
+from harness import DeviceRun, compare, host_inputs, oracle_outputs
 import synth
 from synth import BF16, FP32, GLOBAL, SLIDING, LayerSpec, Workload
 
@@ -53,7 +53,7 @@ def run_paged(w, page, seed, fused=False, softcap=None):
     import mixed_sliding_global_gb300 as g
     hb = host_inputs(w, [0])
     ref = oracle_outputs(w, hb, [0])[0]
-    gr = GpuRun(w, hb)
+    gr = DeviceRun(w, hb)
     spec, d = w.layers[0], gr.dev[0]
     B = len(w.ctx_lens)
     table, n_pages = make_table(B, w.capacity, page, seed)
@@ -137,7 +137,7 @@ def test_bad_page_index_is_reported_not_read():
     spec = LayerSpec(GLOBAL, 0, 16, 1, 512, True)
     w = one_layer(spec, 1, [300, 500], 512)
     hb = host_inputs(w, [0])
-    gr = GpuRun(w, hb)
+    gr = DeviceRun(w, hb)
     d = gr.dev[0]
     table, n_pages = make_table(2, 512, 128, seed=7)
     kp = [to_pool(gr.kc[0], table, n_pages, 128)]

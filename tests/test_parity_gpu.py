@@ -10,7 +10,7 @@ import torch
 
 import synth
 from synth import GLOBAL, SLIDING, BF16, FP32, LayerSpec, Workload
-from harness import GpuRun, compare, host_inputs, oracle_outputs
+from harness import DeviceRun, compare, host_inputs, oracle_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 def run_and_compare(w, layers, seqs=None, q_range=None, max_seq_len=None):
     hb = host_inputs(w, layers, seqs)
     ref = oracle_outputs(w, hb, layers, q_range)
-    gr = GpuRun(w, hb)
+    gr = DeviceRun(w, hb)
     got = {}
     for l in layers:
         if w.is_owner(l):
@@ -141,7 +141,7 @@ def test_ragged_decode_sampled_sequences():
     # the sampled sequences keep their own seeded inputs (seeds depend on the sequence index)
     hb = host_inputs(w, [0, 5], seqs)
     ref = oracle_outputs(hb_w, hb, [0, 5])
-    gr = GpuRun(hb_w, hb)
+    gr = DeviceRun(hb_w, hb)
     for l in (0, 5):
         gr.append(l)
         got = gr.attend(l, max_seq_len=max(lens))
@@ -168,7 +168,7 @@ def test_split_plan_does_not_change_the_result(spec):
     ref = oracle_outputs(w, hb, [0])[0]
     outs = []
     for msl in (5000, 16448):
-        gr = GpuRun(w, hb)
+        gr = DeviceRun(w, hb)
         gr.append(0)
         outs.append(gr.attend(0, max_seq_len=msl))
         torch.cuda.synchronize()
@@ -188,7 +188,7 @@ def test_workspace_is_reusable_across_calls():
         for spec, lens, cap in cases:
             w = one_layer(spec, 1, lens, cap)
             hb = host_inputs(w, [0])
-            gr = GpuRun(w, hb)
+            gr = DeviceRun(w, hb)
             gr.append(0)
             fresh = gr.attend(0)
             d = gr.dev[0]
@@ -210,7 +210,7 @@ def test_ragged_decode_full_batch_sliding_layer():
     lens = w.ctx_lens
     seqs = sorted({lens.index(min(lens)), lens.index(max(lens)), 7, 33, 63})
     hb = host_inputs(w, [0])
-    gr = GpuRun(w, hb)
+    gr = DeviceRun(w, hb)
     gr.append(0)
     got = gr.attend(0, max_seq_len=max(lens))
     torch.cuda.synchronize()

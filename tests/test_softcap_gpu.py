@@ -4,7 +4,7 @@ path. Queries are scaled by powers of two (exact in bf16) so that the cap satura
 import pytest
 import torch
 
-from harness import GpuRun, compare, host_inputs, oracle_outputs
+from harness import DeviceRun, compare, host_inputs, oracle_outputs
 from synth import BF16, FP32, GLOBAL, SLIDING, LayerSpec, Workload
 
 pytestmark = pytest.mark.gpu
@@ -18,7 +18,7 @@ def run(w, softcap, q_gain):
     hb = host_inputs(w, [0])
     hb[0].q.mul_(q_gain)
     ref = oracle_outputs(w, hb, [0], softcap=softcap)[0]
-    gr = GpuRun(w, hb)
+    gr = DeviceRun(w, hb)
     gr.append(0)
     got = gr.attend(0, softcap=softcap)
     torch.cuda.synchronize()
@@ -52,7 +52,7 @@ def test_softcap_fp32_debug_path():
 def test_softcap_zero_is_the_plain_call():
     w = one_layer(LayerSpec(GLOBAL, 0, 16, 1, 512, True), 64, [500, 128], 512)
     hb = host_inputs(w, [0])
-    gr = GpuRun(w, hb)
+    gr = DeviceRun(w, hb)
     gr.append(0)
     plain = gr.attend(0)
     zero = gr.attend(0, softcap=0.0)
