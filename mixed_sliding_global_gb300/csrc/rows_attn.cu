@@ -37,6 +37,7 @@ constexpr int kMaxStages = 8;
 #define GEMMA_ROWS_MIN_BLOCKS 2
 #endif
 constexpr int kSmemBudget = GEMMA_ROWS_SMEM_BUDGET;
+constexpr float kLazyRescaleLog2 = 8.f;  // move the softmax reference only past this growth
 
 template <int D>
 struct RowsLayout {
@@ -329,13 +330,24 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
                 if (!valid) sv = -INFINITY;
                 else if (p.softcap > 0.f) sv = p.cap_log2 * tanhf(sv * p.cap_inner);
                 else sv *= p.scale_log2;
-                const float m_new = fmaxf(m_run[rr], warp_max(sv));
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                const float alpha = exp2f(m_run[rr] - m_use);
-                const __nv_bfloat16 pb = __float2bfloat16_rn(exp2f(sv - m_use));
+                // exponentials against the running reference maximum while the tile maximum
+                // is reduced; the reference moves (and the row is recomputed) only when the
+                // tile maximum exceeds it by more than 2^8, so the result is unchanged (the
+                // final division uses the same reference) and the common tile has no
+                // maximum -> exponential dependency. l is kept per lane (every lane's share is
+                // rescaled alike) and summed over the warp once, at the end.
+                const float m_old = m_run[rr];
+                float pe = exp2f(sv - (m_old == -INFINITY ? 0.f : m_old));
+                const float mx = warp_max(sv);
+                float alpha = 1.f;
+                if (mx > m_old + kLazyRescaleLog2) {  // the same decision in every lane
+                    alpha = exp2f(m_old - mx);         // 0 while the reference is -inf
+                    m_run[rr] = mx;
+                    pe = exp2f(sv - mx);
+                }
+                const __nv_bfloat16 pb = __float2bfloat16_rn(pe);
                 sP[r * Lay::P_STRIDE + lane] = pb;
-                l_run[rr] = l_run[rr] * alpha + warp_sum(__bfloat162float(pb));
-                m_run[rr] = m_new;
+                l_run[rr] = l_run[rr] * alpha + __bfloat162float(pb);
                 if (lane == 0) sAlpha[r] = alpha;
             }
         }
@@ -394,9 +406,12 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         const int r = warp + 8 * rr;
-        if (r < n_rows && lane == 0) {
-            sM[r] = m_run[rr];
-            sL[r] = l_run[rr];
+        if (r < n_rows) {  // the same in every lane of the warp
+            const float lt = warp_sum(l_run[rr]);
+            if (lane == 0) {
+                sM[r] = m_run[rr];
+                sL[r] = lt;
+            }
         }
     }
     named_bar_sync(1, kConsumerWarps * 32);
