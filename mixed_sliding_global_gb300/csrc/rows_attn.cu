@@ -356,12 +356,14 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
         // (3) O = diag(alpha) O + P V over this warp's columns [warp*D/8, +D/8)
         {
             const float a_lo = sAlpha[g], a_hi = sAlpha[g + 8];
+            if (a_lo != 1.f || a_hi != 1.f) {  // the reference moved for one of these rows
 #pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                o[j][0] *= a_lo;
-                o[j][1] *= a_lo;
-                o[j][2] *= a_hi;
-                o[j][3] *= a_hi;
+                for (int j = 0; j < NB; ++j) {
+                    o[j][0] *= a_lo;
+                    o[j][1] *= a_lo;
+                    o[j][2] *= a_hi;
+                    o[j][3] *= a_hi;
+                }
             }
 #pragma unroll
             for (int kk = 0; kk < T / 16; ++kk) {
