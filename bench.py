@@ -47,8 +47,8 @@ PAGE_EXAMPLE = 256      # keys per page of the paged pools
 # captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-40 sliding layer in the
 # unsplit launch configuration of the batch-64 one, and a batch-64 global layer); used only
 # while the kernel sources hash to the recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": "5e6ce76e85e8738c22b63d6095068cfcd49e86be",
-                      "per_algorithmic_byte": {"sliding": 1.0152, "global": 1.0350}}
+NCU_DECODE_TRAFFIC = {"source_sha1": "d608fb587e0e473cd100d8450436aa145e46bc9a",
+                      "per_algorithmic_byte": {"sliding": 1.0152, "global": 1.0351}}
 
 
 # ---------------------------------------------------------------------------------------------
