@@ -196,3 +196,19 @@ def test_paged_argument_checks():
              1, 64, 1, 0, None, None) == UNSUPPORTED
     assert lib().gemma_attn_workspace_size_paged(1, 2, 512, 4, 1, 64, 64, 1) == \
         ctypes.c_size_t(-1).value
+
+
+def test_binding_signatures_match_the_header():
+    """Every prototype in include/gemma_attn.h has as many parameters as the binding's ctypes
+    signature of the same name (an ABI change cannot silently misalign the marshalling)."""
+    import re
+    with open(binding._build.HEADER) as f:
+        text = f.read()
+    protos = re.findall(r"^\s*(?:int|size_t|const char\*)\s+(gemma_\w+)\s*\(([^)]*)\)\s*;",
+                        text, re.M | re.S)
+    assert len(protos) == len(g.exported_symbols())
+    for name, params in protos:
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert name in binding._SIGNATURES, name
+        assert len(binding._SIGNATURES[name][1]) == n, (name, n, len(binding._SIGNATURES[name][1]))
