@@ -43,10 +43,10 @@ BUCKET_REAL_EXAMPLE = [512, 384, 256, 128]   # real rows per sequence of the pad
 RING_EXAMPLE = 1024     # ring slots of the sliding layers' caches (the 12B window)
 PAGE_EXAMPLE = 256      # keys per page of the paged pools
 
-# dram bytes (read + write) per algorithmic byte of the decode row kernel, from the ncu
-# captures summarised in profiles/rows_attn_bf16_decode_*.md (a batch-40 sliding layer in the
-# unsplit launch configuration of the batch-64 one, and a batch-64 global layer); used only
-# while the kernel sources hash to the recorded value
+# dram bytes (read + write) per algorithmic byte of the decode row kernel, from one ncu capture
+# of each launch kind (a batch-40 sliding layer in the unsplit launch configuration of the
+# batch-64 one, and a batch-64 global layer); used only while the kernel sources hash to the
+# recorded value
 NCU_DECODE_TRAFFIC = {"source_sha1": "d608fb587e0e473cd100d8450436aa145e46bc9a",
                       "per_algorithmic_byte": {"sliding": 1.0152, "global": 1.0351}}
 

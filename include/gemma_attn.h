@@ -142,12 +142,15 @@ int gemma_attn_decode(void* out, const void* q, const void* const* k_cache,
  * whose host owns every device allocation, or a latency-critical path that must not call the
  * driver's allocator). Its split scratch is a fixed 64 MiB array compiled into the library,
  * held by every GPU that loads the library until the process exits. It allocates nothing.
- *  - Arguments and results are those of gemma_attn_decode minus workspace/workspace_bytes.
- *  - Returns GEMMA_ERR_WORKSPACE when gemma_attn_workspace_size(...) for these arguments is
- *    larger than 64 MiB (e.g. batch 64 x 16 query heads of head_dim 512 split 19 ways needs
- *    about 40 MB and fits).
- *  - The first call on each device looks up the array's device address (with that device
- *    current); make that first call before any stream capture.
+ *  - Arguments and results are those of gemma_attn_decode minus workspace/workspace_bytes,
+ *    with the same statuses in the same order of checks: an unsupported shape gives
+ *    GEMMA_ERR_UNSUPPORTED, a bad argument GEMMA_ERR_INVALID_ARG or GEMMA_ERR_CAPACITY.
+ *  - Returns GEMMA_ERR_WORKSPACE, with no launch, when the arguments are valid but
+ *    gemma_attn_workspace_size(...) for them is larger than 64 MiB (e.g. batch 64 x 16 query
+ *    heads of head_dim 512 split 19 ways needs about 40 MB and fits).
+ *  - The first call in each CUDA context (per device, and again after a device reset) looks up
+ *    the array's device address with that device current; make that first call before any
+ *    stream capture.
  *  - All calls share the array, which keeps the previous call's contents (nothing in it has to
  *    start at zero); calls whose kernels overlap on the GPU race on it, so the caller must
  *    order them (one stream, or events between streams).

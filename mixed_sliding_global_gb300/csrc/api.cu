@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/gemma_attn.h: host-side validation, owner-layer
 // resolution, the split plan of the decode bucket, and kernel launches. Nothing here
 // allocates memory or synchronises; every launch goes to the caller's stream.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -26,15 +27,20 @@ constexpr long long kNoSplitUnitsPerSm = 2;
 constexpr long long kNoSplitMaxKeys = 2048;
 constexpr long long kSplitCtasPerSm = GEMMA_SPLIT_CTAS_PER_SM;
 
+// SM count of the current device, cached per device (atomics: calls may come from several
+// host threads; they all store the same value)
 int sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
         return -1;
-    if (dev >= 0 && dev < 64) cache[dev] = n;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -20,6 +20,8 @@
 //    (2) per-row online softmax in exp2 form with warp shuffles, P rounded to bf16,
 //    (3) O = diag(alpha) O + P V (warps split head_dim);
 //  - fp32 accumulation throughout; partial (m, l, O) per chunk when the keys are split.
+#include <atomic>
+
 #include "attn_internal.h"
 #include "common.cuh"
 #include "tc.cuh"
@@ -648,13 +650,17 @@ size_t rows_bf16_smem_bytes(int head_dim, int k_eq_v, int* n_stages) {
 
 template <int D>
 static cudaError_t launch_bf16_d(const RowsParams& p, dim3 grid, size_t smem, cudaStream_t st) {
-    static bool configured = false;  // attribute set once per process (same value every time)
-    if (!configured) {
+    // attribute set once per device (the same value every time, so concurrent first calls
+    // from several host threads are harmless)
+    static std::atomic<bool> configured[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(rows_attn_bf16_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);
         if (e != cudaSuccess) return e;
-        configured = true;
+        if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_relaxed);
     }
     CUtensorMap km, vm;
     // [rows][slots][D]: rows = sequences x KV heads (pages x KV heads for a paged pool)

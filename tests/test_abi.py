@@ -212,3 +212,31 @@ def test_binding_signatures_match_the_header():
         n = 0 if params in ("", "void") else params.count(",") + 1
         assert name in binding._SIGNATURES, name
         assert len(binding._SIGNATURES[name][1]) == n, (name, n, len(binding._SIGNATURES[name][1]))
+
+
+def decode_static(owner=(0,), layer=0, max_seq_len=64, batch=1, kind=1, window=0, n_q=4, n_kv=1,
+                  d=64, k_eq_v=1, cap=64, scale=0.125, dtype=0, kc=(FAKE,), vc=(None,)):
+    return lib().gemma_attn_decode_static(FAKE, FAKE, _ptrs(*kc), _ptrs(*vc), _i32(*owner),
+                                          len(owner), layer, FAKE, max_seq_len, batch, kind,
+                                          window, n_q, n_kv, d, k_eq_v, cap, scale, dtype, None,
+                                          None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(d=96), UNSUPPORTED),
+    (dict(n_q=64, n_kv=2), UNSUPPORTED),                 # group of 32
+    (dict(owner=(1,)), INVALID),
+    (dict(max_seq_len=65), CAPACITY),
+    (dict(k_eq_v=0), INVALID),                           # V cache missing
+    (dict(scale=0.0), INVALID),
+    (dict(batch=-1), INVALID),
+])
+def test_static_decode_reports_the_statuses_of_the_workspace_decode(kwargs, status):
+    """The allocation-free decode returns what gemma_attn_decode returns for the same bad
+    arguments (no GPU is touched: every check fails on the host first)."""
+    assert decode_static(**kwargs) == status
+    assert decode(**kwargs) == status
+
+
+def test_static_decode_empty_batch_is_ok():
+    assert decode_static(batch=0) == 0

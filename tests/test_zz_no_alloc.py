@@ -1,10 +1,10 @@
 """GPU: the allocation-free decode entry point gives the results of the workspace one.
 
 gemma_attn_decode_static serves callers that cannot allocate device memory: it takes its split
-scratch from an array built into the library. Two calls in a row with different inputs (so the
-shared scratch carries the first call's data into the second) must each match
-gemma_attn_decode with a caller workspace, within the bf16 tolerance of the parity tests. The
-file is named to be collected last.
+scratch from an array built into the library. Two calls in a row with different inputs and
+split plans (so the shared scratch carries the first call's data into the second) must each
+match gemma_attn_decode with a caller workspace, within the bf16 tolerance of the parity tests.
+The file is named to be collected last.
 """
 import pytest
 import torch
@@ -35,14 +35,18 @@ def _caches(kc, vc):
     return [kc], [vc]
 
 
-@pytest.mark.parametrize("spec,lens,cap", [
-    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), [3000, 5000, 777], 5056),
-    (LayerSpec(SLIDING, 1024, 16, 8, 256, False), [4000, 1500], 4032),
+# Two calls in a row per layer kind: the first with a large split plan (more sequences, longer
+# contexts, more chunks), the second with a smaller plan whose chunks fall elsewhere in the
+# shared array, so partial results the first call left behind would be read by the second if
+# the kernels did not write every partial before reading it.
+@pytest.mark.parametrize("spec,calls,cap", [
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), [([3000, 5000, 777, 4100], 11), ([700], 12)], 5056),
+    (LayerSpec(SLIDING, 1024, 16, 8, 256, False), [([4000, 1500, 3000], 11), ([1100], 12)], 4032),
 ])
-def test_static_scratch_decode_matches_workspace_decode(spec, lens, cap):
+def test_static_scratch_decode_matches_workspace_decode(spec, calls, cap):
     import mixed_sliding_global_gb300 as g
-    outs = []
-    for call, seed in enumerate((11, 12)):                 # two calls in a row
+    outs, plans = [], []
+    for call, (lens, seed) in enumerate(calls):
         w, q, kc, vc, sl = _inputs(spec, lens, cap, seed)
         msl = max(lens)
         kcs, vcs = _caches(kc, vc)
@@ -51,7 +55,9 @@ def test_static_scratch_decode_matches_workspace_decode(spec, lens, cap):
         ws_n = g.gemma_attn_workspace_size(len(lens), spec.kind, spec.window, spec.n_q,
                                            spec.n_kv, spec.head_dim, msl, 1)
         assert ws_n > 0, "the case must use split scratch"
-        ws = torch.zeros(ws_n, dtype=torch.uint8, device="cuda")
+        plans.append(ws_n)
+        # the workspace decode reads only what it wrote: a NaN-filled workspace must not matter
+        ws = torch.full((ws_n // 4,), float("nan"), dtype=torch.float32, device="cuda")
         ref = torch.empty_like(q)
         got = torch.full_like(q, float("nan"))
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -59,11 +65,11 @@ def test_static_scratch_decode_matches_workspace_decode(spec, lens, cap):
         g.gemma_attn_decode_static(got, q, kcs, vcs, [0], 0, sl, msl, device_error=err, **kw)
         torch.cuda.synchronize()
         assert err.item() == 0
-        assert torch.isfinite(got.float()).all()
+        assert torch.isfinite(ref.float()).all() and torch.isfinite(got.float()).all()
         diff = (got.float() - ref.float()).abs()
         assert diff.max().item() <= MAX_ABS and diff.mean().item() <= MEAN_ABS, (call, diff.max())
         outs.append(got)
-    assert not torch.equal(outs[0], outs[1])
+    assert plans[0] > plans[1], "the first call's plan must be the larger one"
 
 
 def test_static_scratch_rejects_oversized_plans():
