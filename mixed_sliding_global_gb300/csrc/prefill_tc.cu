@@ -1,40 +1,51 @@
 // prefill_tc.cu -- prefill-bucket attention on 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// Computes, for a tile of 128 query rows (rows = (token, head of the GQA group) pairs, token
+// Computes, for tiles of 128 query rows (rows = (token, head of the GQA group) pairs, token
 // major, so every row of a tile reads the same KV head), softmax(scale * Q K^T) V over the
 // causal (and, on sliding layers, windowed) key range of each row, with the K/V cache of the
 // owner layer ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", sections 2.1-2.3; the
 // pages' "eager" matmul-softmax-matmul definition, section 4.3).
 //
-// Each CTA has 6 warps:
-//   warps 0-3  softmax: thread r owns row r (TMEM lane r): loads its Q row into TMEM, reads
-//              its S row from TMEM, masks by index, keeps (m, l), writes bf16 P to shared
-//              memory, rescales its O row in TMEM when the running max grows by more than
-//              2^8 (lazy rescaling keeps the result exact: the final division uses the same
-//              reference max), and finally writes O / l.
-//   warp 4     TMA producer: streams 128-key K and V tiles (128-byte swizzle, one box per
-//              64 columns of head_dim) through a ring of shared-memory slots.
-//   warp 5     MMA issuer: S = Q K^T (A = Q from TMEM, B = K, K-major) and O += P V (A = P,
-//              K-major, B = V, MN-major), fp32 accumulation in TMEM; tcgen05.commit signals
-//              the mbarriers that order the warps.
-// TMEM (512 columns): Q (DH/2 columns of packed bf16), S (128), O (DH), DH = head_dim / CL.
+// Persistent grid: one CTA (head_dim 512: one 2-CTA cluster) per SM walks work units = (row
+// tile, sequence, KV head), latest row tiles (longest key ranges) first, and within a unit
+// 64-key tiles. The tiles of all its units form one flat sequence T = 0, 1, 2, ... per CTA.
+// Each CTA has 10 warps:
+//   warps 0-3 / 4-7   softmax warpgroups WG0 / WG1: WG (T % 2) handles tile T; thread r owns
+//              row r (TMEM lane r). It reads S(T) from TMEM, masks by index, hands the row's
+//              running softmax reference to the other group (the reference moves only when a
+//              tile maximum exceeds it by more than 2^8: lazy rescaling keeps the result exact,
+//              the final division uses the same reference), writes bf16 P to shared memory,
+//              and rescales the O row in TMEM when the reference moved. The group that handles
+//              a unit's first tile loads the unit's Q rows into TMEM; both groups write O / l.
+//   warp 8     TMA producer: 64-key K and V tiles (128-byte swizzle, one box per 64 columns of
+//              head_dim) into a FIFO ring of shared-memory slots, in the MMA warp's order.
+//   warp 9     MMA issuer: step i issues S(i) = Q K(i)^T (A = Q from TMEM, B = K, K-major) into
+//              TMEM buffer i % 2 and O += P(i-2) V(i-2) (A = P, K-major, B = V, MN-major), so
+//              the softmax of a tile overlaps two later tiles' tensor work.
+// Synchronisation is per step (rings of 8 mbarriers): step_ready[i] completes when the step's
+// K/V tiles have landed and P(i-2) is written; the MMA warp commits step_done[i] after the
+// step's MMAs. A tcgen05.mma is accepted only when the one before it is nearly done, so each
+// wait or commit between MMA groups idles the tensor core: the MMA warp does one of each per
+// step.
+// TMEM (512 columns): Q (DH/2 columns of packed bf16) at 0, S buffers at 128 and 192 (64 fp32
+// columns each), O (DH columns) at 256; DH = head_dim / CL.
 //
 // CL = 2 (head_dim 512): a 128 x 512 fp32 O alone would fill the 512 TMEM columns of an SM,
 // so a cluster of two CTAs splits head_dim: CTA h holds Q[:, 256h:256h+256] and reads only
 // that half of K and V. Each computes a partial S over its half, sends it to its peer through
 // distributed shared memory, and adds the peer's partial to its own; each then accumulates and
 // writes its own half of O with its own P, m and l. No multiply-add is done twice. With k_eq_v
-// the K half is also the V half.
-// The partial scores travel as fp16 (saturating): the exchange, not the tensor core, bounds
-// these clusters, and fp16 halves its bytes. Each CTA keeps its own partial in fp32; the peer's
-// rounding moves a score by at most 2^-11 of its partial (for |partial| <= 128 raw, <= 0.06 raw,
-// i.e. < 0.4% in exp(scale * s) at scale 1/sqrt(512)), the size of the bf16 rounding P already
-// gets before P V.
+// the K half is also the V half. The partial scores travel as fp16 (saturating) with
+// asynchronous stores into the peer's shared memory (st.async, completion counted in bytes on
+// the peer's mbarrier); each CTA keeps its own partial in fp32, so the peer's rounding moves a
+// score by at most 2^-11 of its partial.
 //
-// The key range of the tile is clamped to [first row's window start, last row's position]
-// before any load; rows of the last partial key tile beyond the range are zeroed in shared
-// memory before they enter P V.
+// The key range of a unit is clamped to [first row's window start, last row's position] before
+// any load; rows of a K/V tile outside the range are zeroed in shared memory before they enter
+// P V (they may hold anything, NaN included).
 #include <cuda_fp16.h>
+
+#include <atomic>
 
 #include "attn_internal.h"
 #include "tc.cuh"
@@ -42,28 +53,40 @@
 
 namespace gemma {
 
-constexpr int kTcThreads = 192;
-constexpr int kTcMaxSlots = 8;
-constexpr int kTcKeys = 128;                   // keys per tile (N of S = Q K^T)
-constexpr int kTcSmemLimit = 232448;           // max dynamic shared memory per block (sm_100)
+constexpr int kFaWarps = 10;
+constexpr int kFaThreads = kFaWarps * 32;
+constexpr int kFaProducerWarp = 8;
+constexpr int kFaMmaWarp = 9;
+constexpr int kFaMaxSlots = 8;
+constexpr int kFaSteps = 8;                   // entries of the per-step barrier rings
+constexpr int kFaKeys = 64;                   // keys per tile (N of S = Q K^T)
+constexpr int kFaSmemLimit = 232448;          // max dynamic shared memory per block
 constexpr float kLazyRescaleLog2 = 8.f;
 
-struct TcParams {
-    RowsParams p;
-    int n_slots;
-};
-
 template <int D, int CL>
-struct TcLayout {
+struct FaLayout {
     static constexpr int DH = D / CL;                    // head_dim columns owned by a CTA
     static constexpr int CHUNKS = DH / 64;               // 64-column boxes per K/V tile
-    static constexpr int SLOT = CHUNKS * kTcKeys * 128;  // bytes of one K or V tile
-    static constexpr int P_BYTES = kTcKeys * 128 * 2;    // 128 rows x 128 keys bf16
-    static constexpr int X_BYTES = CL > 1 ? 128 * kTcKeys * 2 : 0;  // peer's partial S (fp16)
+    static constexpr int BOX = kFaKeys * 128;            // one box: 64 keys x 64 columns
+    static constexpr int SLOT = CHUNKS * BOX;            // one K or V tile
+    static constexpr int P_TILE = 128 * kFaKeys * 2;     // 128 rows x 64 keys bf16
+    static constexpr int X_TILE = CL > 1 ? 128 * kFaKeys * 2 : 0;  // peer's partial S (fp16)
     static constexpr int Q_COL = 0;                      // TMEM columns
-    static constexpr int S_COL = 128;
+    static constexpr int S_COL = 128;                    // + 64 * buffer
     static constexpr int O_COL = 256;
-    static_assert(DH / 2 <= 128 && 256 + DH <= 512, "TMEM budget");
+    // fixed shared memory besides the ring: P (2), X (2), reference row maxima, barriers
+    static constexpr int FIXED = 2 * P_TILE + 2 * X_TILE + 512 + 512;
+    static_assert(DH / 2 <= 128 && O_COL + DH <= 512, "TMEM budget");
+    static_assert(2 * 128 * 8 <= P_TILE, "the epilogue's (m, l) exchange fits in one P buffer");
+};
+
+struct FaParams {
+    RowsParams p;
+    int n_slots;
+    int batch;
+    int n_rt;      // row tiles per (sequence, KV head)
+    int n_units;   // n_rt * batch * n_kv
+    int n_workers; // CTAs (clusters) walking the units
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -82,10 +105,15 @@ GEMMA_DEVINL uint32_t map_to_peer(const void* local, uint32_t peer) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(peer));
     return r;
 }
-GEMMA_DEVINL void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-                 "r"(c), "r"(d)
-                 : "memory");
+// Asynchronous 16-byte store into the peer CTA's shared memory; its completion counts 16 bytes
+// of transactions on the peer's mbarrier `mbar` (both cluster shared-memory addresses).
+GEMMA_DEVINL void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                              uint32_t mbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+            "r"(addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(mbar)
+        : "memory");
 }
 // two fp32 -> packed fp16 (lo in the low half), round to nearest; values beyond the fp16
 // range saturate to +-65504 instead of becoming infinite
@@ -98,8 +126,11 @@ GEMMA_DEVINL float2 unpack_f16(uint32_t v) {
     __half2 h = *reinterpret_cast<__half2*>(&v);
     return __half22float2(h);
 }
-GEMMA_DEVINL void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+// Arrival on the peer CTA's mbarrier without release ordering: used only after loads whose
+// values have already been consumed (so the reads are complete), where a release would also
+// wait for this thread's outstanding asynchronous stores to the peer.
+GEMMA_DEVINL void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 GEMMA_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -125,81 +156,176 @@ GEMMA_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* er
         }
     }
 }
+// Adds `bytes` to the transaction count the current phase of `bar` waits for.
+GEMMA_DEVINL void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// `count` arrivals on `bar` at once.
+GEMMA_DEVINL void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+// 1 / x (hardware approximation; 1 / +inf = +0)
+GEMMA_DEVINL float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------------------------------------
+// work units
+// ---------------------------------------------------------------------------------------------
+struct FaUnit {
+    int b, kvh, rt, row0;
+    int n_rows;       // rows of the bucket this unit writes
+    int n_rows_real;  // rows that attend (the rest are pad rows or a bad sequence: zeros)
+    int len, n_real;
+    bool bad, bad_real;
+    int k_begin, k_end, n_tiles;
+    int n_head;       // leading keys of the first tile before every row's window (aligned start)
+};
+
+// Unit u: row tiles from the last (longest key ranges) to the first, then sequences, then KV
+// heads.
+GEMMA_DEVINL FaUnit fa_unit(const FaParams& fp, int u) {
+    const RowsParams& p = fp.p;
+    FaUnit U;
+    const int per_rt = fp.batch * p.n_kv;
+    const int q = u / per_rt, rem = u - q * per_rt;
+    U.rt = fp.n_rt - 1 - q;
+    U.b = rem / p.n_kv;
+    U.kvh = rem - U.b * p.n_kv;
+    const int rows_total = p.n_tok * p.G;
+    U.row0 = U.rt * 128;
+    U.n_rows = min(128, rows_total - U.row0);
+    U.len = __ldg(p.seq_lens + U.b);
+    // real tokens of this sequence (a padded bucket's first n_real rows; all rows otherwise);
+    // the i-th real token sits at len - n_real + i, the pad rows' outputs are zero
+    U.n_real = p.n_real ? __ldg(p.n_real + U.b) : p.n_tok;
+    U.bad_real = U.n_real < 0 || U.n_real > p.n_tok;
+    U.bad = U.bad_real || U.len < U.n_real || (!p.ring && U.len > p.cap) || U.len > p.max_seq_len;
+    U.n_rows_real = U.bad ? 0 : max(0, min(128, U.n_real * p.G - U.row0));
+    // key range: from the first row's window start to the last real row's position (a ring
+    // cache's or paged pool's tiles start at multiples of the tile, so that none wraps around
+    // the ring or crosses a page; the rows' masks drop the keys before the window)
+    const int tok_first = U.row0 / p.G;
+    const int tok_last = (U.row0 + max(U.n_rows_real, 1) - 1) / p.G;
+    const int pos_first = U.len - U.n_real + tok_first;
+    const int lo_first = p.is_sliding ? max(0, pos_first - p.window + 1) : 0;
+    U.k_begin = (p.ring || p.page_size) ? (lo_first & ~(kFaKeys - 1)) : lo_first;
+    U.k_end = U.len - U.n_real + tok_last + 1;
+    U.n_tiles = U.n_rows_real == 0 ? 0 : (U.k_end - U.k_begin + kFaKeys - 1) / kFaKeys;
+    U.n_head = lo_first - U.k_begin;
+    return U;
+}
+
+// One tile of the flat per-CTA sequence, as the producer and the MMA warp see it.
+struct FaTile {
+    bool valid, first, last;
+    int ord;       // ordinal of its unit among this CTA's units that have tiles
+    int n_valid;   // keys of the tile inside the unit's range (the rest are zeroed)
+    int n_head;    // leading keys zeroed (first tile of an aligned-start unit)
+    int key0;      // first key
+    int b, kvh;
+    int slot;      // ring slot holding it (k_eq_v: K and V)
+};
+
+// Walks this CTA's units and their tiles in order.
+struct FaTileIter {
+    int u, stride, t, ord;
+    FaUnit U;
+    GEMMA_DEVINL void init(const FaParams& fp, int worker) {
+        u = worker;
+        stride = fp.n_workers;
+        t = 0;
+        ord = -1;
+        U.n_tiles = 0;
+        U.b = U.kvh = 0;
+        U.k_begin = 0;
+        u -= stride;  // next() advances to the first unit
+    }
+    GEMMA_DEVINL FaTile next(const FaParams& fp) {
+        FaTile T;
+        T.valid = false;
+        while (t >= U.n_tiles) {
+            u += stride;
+            if (u >= fp.n_units) return T;
+            U = fa_unit(fp, u);
+            t = 0;
+            if (U.n_tiles > 0) ++ord;
+        }
+        T.valid = true;
+        T.first = t == 0;
+        T.last = t == U.n_tiles - 1;
+        T.ord = ord;
+        T.key0 = U.k_begin + t * kFaKeys;
+        T.n_valid = min(kFaKeys, U.k_end - T.key0);
+        T.n_head = t == 0 ? U.n_head : 0;
+        T.b = U.b;
+        T.kvh = U.kvh;
+        T.slot = 0;
+        ++t;
+        return T;
+    }
+};
 
 // SOFTCAP: the soft-capped variant (a separate instantiation, so that the plain kernel carries
 // no code for it)
 template <int D, int CL, bool SOFTCAP>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kFaThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap, const TcParams tp) {
+                      const __grid_constant__ CUtensorMap vmap, const FaParams fp) {
     pdl_launch_dependents();
     pdl_wait();  // the previous kernel on the stream has completed
-    using Lay = TcLayout<D, CL>;
+    using Lay = FaLayout<D, CL>;
     constexpr int DH = Lay::DH;
-    const RowsParams& p = tp.p;
+    const RowsParams& p = fp.p;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int NS = tp.n_slots;
+    const int NS = fp.n_slots;
     uint8_t* slots = smem;
-    uint8_t* sP = smem + NS * Lay::SLOT;
-    float* sX = reinterpret_cast<float*>(sP + Lay::P_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + Lay::P_BYTES + Lay::X_BYTES);
-    uint64_t* kv_full = bars;
-    uint64_t* kv_empty = bars + kTcMaxSlots;
-    uint64_t* q_ready = bars + 2 * kTcMaxSlots;
-    uint64_t* s_full = q_ready + 1;
-    uint64_t* s_free = q_ready + 2;
-    uint64_t* p_full = q_ready + 3;
-    uint64_t* o_done = q_ready + 4;
-    uint64_t* x_full = q_ready + 5;  // the peer's partial S has landed in sX
-    uint64_t* x_free = q_ready + 6;  // the peer has read the partial S this CTA sent it
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(q_ready + 7);
-
+    uint8_t* sP = smem + NS * Lay::SLOT;                     // P buffers [2][128 x 64] bf16
+    uint8_t* sX = sP + 2 * Lay::P_TILE;                      // peer partials [2][8][128] x 16 B
+    float* mref = reinterpret_cast<float*>(sX + 2 * Lay::X_TILE);  // [128] softmax references
+    uint64_t* bars = reinterpret_cast<uint64_t*>(mref + 128);
+    // Step i of the MMA warp issues S(i) and P V(i-2). step_ready[i % R] completes when the
+    // step's K/V tiles have landed (producer arrival + transaction bytes) and P(i-2) is in
+    // shared memory (4 warp arrivals of the softmax group; the producer arrives for them when
+    // the step has no P V). step_done[i % R] is committed after the step's MMAs: S(i) is in
+    // TMEM, P V(i-2) has completed (so P buffer i % 2 and the step's ring slots are free).
+    uint64_t* step_ready = bars;
+    uint64_t* step_done = bars + kFaSteps;
+    uint64_t* x_full = bars + 2 * kFaSteps;     // [2] the peer's partial S for group w landed
+    uint64_t* x_free = x_full + 2;              // [2] the peer has read what this CTA sent it
+    uint64_t* o_full = x_full + 4;              // a unit's last P V has completed
+    uint64_t* o_free = x_full + 5;              // the epilogue has read O
+    uint64_t* q_ready = x_full + 6;             // a unit's Q is in TMEM
+    uint64_t* m_ready = x_full + 7;             // the reference after tile T is in mref
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(x_full + 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t h = CL > 1 ? cluster_rank() : 0u;  // which head_dim part this CTA owns
-    const int rt = blockIdx.x / CL, kvh = blockIdx.y, b = blockIdx.z;
-    const int rows_total = p.n_tok * p.G;
-    const int row0 = rt * 128;
-    const int n_rows = min(128, rows_total - row0);  // rows of the bucket this CTA writes
-    const int len = __ldg(p.seq_lens + b);
-    // real tokens of this sequence (a padded bucket's first n_real rows; all rows otherwise);
-    // the i-th real token sits at len - n_real + i, the pad rows' outputs are zero
-    const int n_real = p.n_real ? __ldg(p.n_real + b) : p.n_tok;
-    const bool bad_real = n_real < 0 || n_real > p.n_tok;
-    const bool bad = bad_real || len < n_real || (!p.ring && len > p.cap) || len > p.max_seq_len;
-    const int n_rows_real = bad ? 0 : max(0, min(128, n_real * p.G - row0));  // rows that attend
+    const int worker = blockIdx.x / CL;
 
-    // key range of the tile: from the first row's window start to the last real row's position
-    const int tok_first = row0 / p.G, tok_last = (row0 + max(n_rows_real, 1) - 1) / p.G;
-    const int pos_first = len - n_real + tok_first, pos_last = len - n_real + tok_last;
-    // (a ring cache's tiles start at multiples of the tile, so that none wraps around the ring;
-    // the rows' masks drop the keys before the window)
-    const int k_begin = p.is_sliding ? (max(0, pos_first - p.window + 1) & ((p.ring || p.page_size) ? ~(kTcKeys - 1) : ~0))
-                                     : 0;
-    const int k_end = pos_last + 1;
-    const int n_tiles = n_rows_real == 0 ? 0 : (k_end - k_begin + kTcKeys - 1) / kTcKeys;
-    // K/V ring split: with K = V one ring of NS slots; otherwise NV slots for V (V is needed
-    // only by P V, which comes last) and the rest for K
-    const int NV = p.k_eq_v ? 0 : (NS / 3 > 1 ? NS / 3 : 1);
-    const int NK = NS - NV;
-
-    if (warp == 5) {
+    if (warp == kFaMmaWarp) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int i = 0; i < kFaSteps; ++i) {
+            mbar_init(&step_ready[i], 5);
+            mbar_init(&step_done[i], 1);
         }
-        mbar_init(q_ready, 128);
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 4);
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
-        mbar_init(x_full, 128);
-        mbar_init(x_free, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&x_full[i], 1);  // one local arrival with the exchange's byte count
+            mbar_init(&x_free[i], 4);  // the peer's four warps have read their copy
+        }
+        mbar_init(o_full, 1);
+        mbar_init(o_free, 8);
+        mbar_init(q_ready, 4);
+        mbar_init(m_ready, 128);
         fence_barrier_init();
     }
     tc_fence_before();
@@ -207,353 +333,469 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (CL > 1) cluster_sync();  // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tQ = tmem + Lay::Q_COL, tS = tmem + Lay::S_COL, tO = tmem + Lay::O_COL;
+    const uint32_t tQ = tmem + Lay::Q_COL, tO = tmem + Lay::O_COL;
 
-    if (warp == 4) {
+    if (warp == kFaProducerWarp) {
         // ------------------------------- TMA producer --------------------------------------
-        // K tiles use slots [0, NK), V tiles slots [NK, NS). K runs one tile ahead of V, so a
-        // K slot is refilled as soon as its S = Q K^T finished, independently of P V.
+        // Step i loads K(i) and then (K != V) V(i-2) into the next slots of a FIFO ring. A slot
+        // is reused once the step that last read it has completed (K: its S step; V, or K used
+        // as V: its P V step).
         if (lane == 0) {
-            auto load = [&](const CUtensorMap* map, int slot, int t) {
+            bool ok = true;
+            int ps = 0;
+            int rel[kFaMaxSlots];  // step whose completion frees each slot (-1: free)
+            for (int k = 0; k < kFaMaxSlots; ++k) rel[k] = -1;
+            auto claim = [&](int release_step) -> int {
+                const int s0 = ps;
+                const int r0 = rel[s0];
+                if (r0 >= 0 && ok) ok = mbar_wait(&step_done[r0 % kFaSteps], (r0 / kFaSteps) & 1, p.err);
+                rel[s0] = release_step;
+                if (++ps == NS) ps = 0;
+                return s0;
+            };
+            auto load = [&](const CUtensorMap* map, const FaTile& T, int slot, uint64_t* bar) {
                 uint8_t* dst = slots + slot * Lay::SLOT;
-                mbar_arrive_expect_tx(&kv_full[slot], Lay::SLOT);
                 // cache row and slot of the tile's first key (a bad page index reads zeros)
                 int row3 = 0, slot0 = 0;
-                if (!kv_place(p, b, kvh, k_begin + t * kTcKeys, row3, slot0)) {
+                if (!kv_place(p, T.b, T.kvh, T.key0, row3, slot0)) {
                     report(p.err, GEMMA_DEVERR_PAGE);
                     row3 = p.n_pages * p.n_kv;
                 }
+#pragma unroll
                 for (int c = 0; c < Lay::CHUNKS; ++c)
-                    tma_load_3d(dst + c * kTcKeys * 128, map, (int)h * DH + c * 64, slot0, row3,
-                                &kv_full[slot]);
+                    tma_load_3d(dst + c * Lay::BOX, map, (int)h * DH + c * 64, slot0, row3, bar);
             };
-            bool ok = true;
-            // ring cursors (slot, phase of the current pass, whether a pass has completed):
-            // kept incrementally, no division by the runtime ring sizes
-            int ks = 0, vs = 0;
-            uint32_t kph = 0, vph = 0;
-            bool kwrap = false, vwrap = false;
-            for (int i = 0; i <= n_tiles && ok; ++i) {
-                const int tk = i;          // K tile issued at step i
-                const int tv = i - 1;      // V tile issued at step i
-                if (tk < n_tiles) {
-                    if (kwrap) ok = mbar_wait(&kv_empty[ks], kph ^ 1u, p.err);
-                    if (ok) load(&kmap, ks, tk);
-                    if (++ks == NK) {
-                        ks = 0;
-                        kph ^= 1u;
-                        kwrap = true;
-                    }
+            FaTileIter it;
+            it.init(fp, worker);
+            FaTile h1, h2;
+            h1.valid = h2.valid = false;
+            for (int i = 0;; ++i) {
+                const FaTile cur = it.next(fp);
+                if (!cur.valid && !h1.valid && !h2.valid) break;
+                const bool pv = h2.valid;
+                if (cur.valid || pv) {
+                    const int sk = cur.valid ? claim(p.k_eq_v ? i + 2 : i) : -1;
+                    const int sv = (!p.k_eq_v && pv) ? claim(i) : -1;
+                    // the barrier entry's previous step (i - R) has completed
+                    if (i >= kFaSteps && ok)
+                        ok = mbar_wait(&step_done[i % kFaSteps], ((i - kFaSteps) / kFaSteps) & 1, p.err);
+                    uint64_t* bar = &step_ready[i % kFaSteps];
+                    const uint32_t bytes = (sk >= 0 ? Lay::SLOT : 0) + (sv >= 0 ? Lay::SLOT : 0);
+                    if (bytes) mbar_expect_tx(bar, bytes);
+                    mbar_arrive_cnt(bar, pv ? 1u : 5u);
+                    if (ok && sk >= 0) load(&kmap, cur, sk, bar);
+                    if (ok && sv >= 0) load(&vmap, h2, sv, bar);
                 }
-                if (!p.k_eq_v && tv >= 0 && ok) {
-                    if (vwrap) ok = mbar_wait(&kv_empty[NK + vs], vph ^ 1u, p.err);
-                    if (ok) load(&vmap, NK + vs, tv);
-                    if (++vs == NV) {
-                        vs = 0;
-                        vph ^= 1u;
-                        vwrap = true;
-                    }
-                }
+                h2 = h1;
+                h1 = cur;
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kFaMmaWarp) {
         // -------------------------------- MMA issuer ---------------------------------------
-        const uint32_t id_qk = idesc_bf16(128, kTcKeys, 0, 0);
+        // One wait and one commit per step: an MMA is issued only once the one before it is
+        // nearly done, so every wait or commit between MMA groups idles the tensor core.
+        const uint32_t id_qk = idesc_bf16(128, kFaKeys, 0, 0);
         const uint32_t id_pv = idesc_bf16(128, DH, 0, 1);
-        bool ok = mbar_wait(q_ready, 0, p.err);
-        // rows [0, n_head) of the first tile when it starts before every row's window (a
-        // tile-aligned start): masked keys whose values must not reach P V as 0 * x
-        const int n_head = p.is_sliding ? max(0, max(0, pos_first - p.window + 1) - k_begin) : 0;
-        auto zero_head = [&](uint8_t* tile) {
-            for (int idx = lane; idx < Lay::CHUNKS * n_head * 8; idx += 32) {
-                const int c = idx / (n_head * 8), rem = idx - c * n_head * 8;
-                *reinterpret_cast<uint4*>(tile + c * kTcKeys * 128 + (rem / 8) * 128 +
-                                          (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        };
-        auto zero_tail = [&](uint8_t* tile, int n_valid) {
-            // rows [n_valid, 128) of every 64-column box: whole 128-byte rows, so the
-            // swizzle does not matter
-            const int n_zero = kTcKeys - n_valid;
-            for (int idx = lane; idx < Lay::CHUNKS * n_zero * 8; idx += 32) {
-                const int c = idx / (n_zero * 8), rem = idx - c * n_zero * 8;
-                const int r = n_valid + rem / 8, q16 = rem % 8;
-                *reinterpret_cast<uint4*>(tile + c * kTcKeys * 128 + r * 128 + q16 * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        };
-        // ring cursors of the consumer side: K slot and phase for S = Q K^T, V slot and phase
-        // for P V, and (with K as V) the slot of the previous K tile
-        int mk = 0, mv = 0, k_prev = 0;
-        uint32_t mkph = 0, mvph = 0;
-        auto issue_pv = [&](int j) {
-            if (ok) ok = mbar_wait(p_full, j & 1, p.err);
-            const int sv = p.k_eq_v ? k_prev : NK + mv;
-            const uint32_t sv_phase = mvph;
-            if (!p.k_eq_v && ++mv == NV) {
-                mv = 0;
-                mvph ^= 1u;
-            }
-            if (ok && !p.k_eq_v) {
-                ok = mbar_wait(&kv_full[sv], sv_phase, p.err);
-                const int n_valid = k_end - (k_begin + j * kTcKeys);
-                if (n_valid < kTcKeys) zero_tail(slots + sv * Lay::SLOT, n_valid);
-                if (j == 0 && n_head > 0) zero_head(slots + sv * Lay::SLOT);
-            }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t vbase = smem_u32(slots + sv * Lay::SLOT);
-                const uint32_t pbase = smem_u32(sP);
-#pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    const uint64_t a = smem_desc_sw128(pbase + (kk / 4) * (kTcKeys * 128) +
-                                                           (kk % 4) * 32, 0, 1024);
-                    const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kTcKeys * 128, 1024);
-                    umma_ss(tO, a, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        bool ok = true;
+        int ps = 0;
+        // rows of a tile that must not reach P V (outside the unit's key range): zeroed
+        auto zero_edges = [&](int slot, const FaTile& T) {
+            const int n_tail = kFaKeys - T.n_valid;
+            if (n_tail <= 0 && T.n_head <= 0) return;
+            uint8_t* tile = slots + slot * Lay::SLOT;
+            if (n_tail > 0) {
+                for (int idx = lane; idx < Lay::CHUNKS * n_tail * 8; idx += 32) {
+                    const int c = idx / (n_tail * 8), rem = idx - c * n_tail * 8;
+                    *reinterpret_cast<uint4*>(tile + c * Lay::BOX + (T.n_valid + rem / 8) * 128 +
+                                              (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
-                umma_commit(o_done);
-                umma_commit(&kv_empty[sv]);
             }
+            if (T.n_head > 0) {
+                for (int idx = lane; idx < Lay::CHUNKS * T.n_head * 8; idx += 32) {
+                    const int c = idx / (T.n_head * 8), rem = idx - c * T.n_head * 8;
+                    *reinterpret_cast<uint4*>(tile + c * Lay::BOX + (rem / 8) * 128 +
+                                              (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
             __syncwarp();
         };
-        for (int t = 0; t < n_tiles; ++t) {
-            const int sk = mk;
-            if (ok) ok = mbar_wait(&kv_full[sk], mkph, p.err);
-            if (++mk == NK) {
-                mk = 0;
-                mkph ^= 1u;
-            }
-            if (p.k_eq_v) {
-                const int n_valid = k_end - (k_begin + t * kTcKeys);
-                if (n_valid < kTcKeys) zero_tail(slots + sk * Lay::SLOT, n_valid);
-                if (t == 0 && n_head > 0) zero_head(slots + sk * Lay::SLOT);
-            }
-            if (t >= 1 && ok) ok = mbar_wait(s_free, (t - 1) & 1, p.err);
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t kbase = smem_u32(slots + sk * Lay::SLOT);
+        auto issue_s = [&](const FaTile& T, int i) {  // lane 0: S(i) = Q K(i)^T
+            const uint64_t kd = smem_desc_sw128(smem_u32(slots + T.slot * Lay::SLOT), 0, 1024);
+            const uint32_t tS = tmem + Lay::S_COL + 64 * (i & 1);
 #pragma unroll
-                for (int c = 0; c < Lay::CHUNKS; ++c)
+            for (int c = 0; c < Lay::CHUNKS; ++c)
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        umma_ts(tS, tQ + c * 32 + ks * 8,
-                                smem_desc_sw128(kbase + c * kTcKeys * 128 + ks * 32, 0, 1024),
-                                id_qk, (c | ks) ? 1u : 0u);
-                umma_commit(s_full);
-                if (!p.k_eq_v) umma_commit(&kv_empty[sk]);
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_ts(tS, tQ + c * 32 + ks * 8,
+                            kd + (uint64_t)((c * Lay::BOX + ks * 32) >> 4), id_qk,
+                            (c | ks) ? 1u : 0u);
+        };
+        auto issue_pv = [&](const FaTile& T, int i) {  // lane 0: O (+)= P(i-2) V(i-2)
+            const uint64_t vd = smem_desc_sw128(smem_u32(slots + T.slot * Lay::SLOT), Lay::BOX, 1024);
+            const uint64_t pd = smem_desc_sw128(smem_u32(sP + (i & 1) * Lay::P_TILE), 0, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kFaKeys / 16; ++kk)
+                umma_ss(tO, pd + (uint64_t)((kk * 32) >> 4), vd + (uint64_t)((kk * 2048) >> 4),
+                        id_pv, (!T.first || kk > 0) ? 1u : 0u);
+            if (T.last) umma_commit(o_full);
+        };
+        FaTileIter it;
+        it.init(fp, worker);
+        FaTile h1, h2;
+        h1.valid = h2.valid = false;
+        for (int i = 0;; ++i) {
+            FaTile cur = it.next(fp);
+            if (!cur.valid && !h1.valid && !h2.valid) break;
+            if (cur.valid || h2.valid) {
+                // slots in the producer's order: K(i), then (K != V) V(i-2)
+                if (cur.valid) {
+                    cur.slot = ps;
+                    if (++ps == NS) ps = 0;
+                }
+                if (!p.k_eq_v && h2.valid) {
+                    h2.slot = ps;
+                    if (++ps == NS) ps = 0;
+                }
+                if (ok) ok = mbar_wait(&step_ready[i % kFaSteps], (i / kFaSteps) & 1, p.err);
+                if (p.k_eq_v) {
+                    if (cur.valid) zero_edges(cur.slot, cur);  // the slot also serves as V
+                } else if (h2.valid) {
+                    zero_edges(h2.slot, h2);
+                }
+                // the previous unit's epilogue has read O before this unit's first P V
+                if (h2.valid && h2.first && h2.ord > 0 && ok)
+                    ok = mbar_wait(o_free, (h2.ord - 1) & 1, p.err);
+                tc_fence_after();
+                if (cur.valid && cur.first) {
+                    // a unit's first S: the P V goes first (the previous unit's epilogue waits
+                    // for it, and the group that loads this unit's Q may have to finish that
+                    // epilogue first)
+                    if (h2.valid && lane == 0) issue_pv(h2, i);
+                    __syncwarp();
+                    if (ok) ok = mbar_wait(q_ready, cur.ord & 1, p.err);
+                    tc_fence_after();
+                    if (lane == 0) issue_s(cur, i);
+                } else if (lane == 0) {
+                    if (cur.valid) issue_s(cur, i);
+                    if (h2.valid) issue_pv(h2, i);
+                }
+                if (lane == 0) umma_commit(&step_done[i % kFaSteps]);
+                __syncwarp();
             }
-            __syncwarp();
-            if (t >= 1) issue_pv(t - 1);
-            k_prev = sk;
+            h2 = h1;
+            h1 = cur;
         }
-        if (n_tiles > 0) issue_pv(n_tiles - 1);
     } else {
         // ------------------------------ softmax warps --------------------------------------
-        const int r = threadIdx.x;  // tile row = TMEM lane
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        const bool row_ok = r < n_rows_real;
-        int token = 0, head = 0, lo = 1, hi = 0;
-        if (row_ok) {
-            const int R = row0 + r;
-            token = R / p.G;
-            head = kvh * p.G + (R - token * p.G);
-            const int pos = len - n_real + token;
-            lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
-            hi = pos + 1;
-        }
-        // this CTA's part of the Q row into TMEM (zeros for rows outside the tile)
-        {
-            const uint4* qrow = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                (((size_t)b * p.n_tok + token) * p.n_q + head) * (size_t)D + h * DH);
-#pragma unroll
-            for (int j = 0; j < DH / 64; ++j) {
-                uint32_t v[32];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint4 x = row_ok ? __ldg(qrow + j * 8 + e) : make_uint4(0u, 0u, 0u, 0u);
-                    v[4 * e + 0] = x.x;
-                    v[4 * e + 1] = x.y;
-                    v[4 * e + 2] = x.z;
-                    v[4 * e + 3] = x.w;
-                }
-                tmem_st32(tQ + lane_off + j * 32, v);
-            }
-            tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(q_ready);
-
+        const int w = warp >> 2;               // softmax group: tiles T with T % 2 == w
+        const int r = threadIdx.x & 127;       // tile row = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        uint8_t* sPw = sP + w * Lay::P_TILE;
         uint32_t peer_x = 0, peer_x_full = 0, peer_x_free = 0;
         if (CL > 1) {
-            peer_x = map_to_peer(sX + 4 * r, h ^ 1u);
-            peer_x_full = map_to_peer(x_full, h ^ 1u);
-            peer_x_free = map_to_peer(x_free, h ^ 1u);
+            peer_x = map_to_peer(sX + w * Lay::X_TILE + 16 * r, h ^ 1u);
+            peer_x_full = map_to_peer(&x_full[w], h ^ 1u);
+            peer_x_free = map_to_peer(&x_free[w], h ^ 1u);
         }
-
         bool ok = true;
-        float m_ref = -INFINITY, l = 0.f;
-        for (int t = 0; t < n_tiles; ++t) {
-            if (ok) ok = mbar_wait(s_full, t & 1, p.err);
-            tc_fence_after();
-            float s[kTcKeys];
-#pragma unroll
-            for (int j = 0; j < kTcKeys / 32; ++j) {
-                uint32_t v[32];
-                tmem_ld32(tS + lane_off + j * 32, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) s[j * 32 + e] = __uint_as_float(v[e]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
 
-            if (CL > 1) {
-                // send this row's partial scores to the peer, then add the peer's partial
-                if (t >= 1 && ok) ok = mbar_wait_cluster(x_free, (t - 1) & 1, p.err);
-                // chunk-major layout X[c][r] (16-byte chunks of 8 fp16 scores): a warp's 32
-                // stores of chunk c are one contiguous 512-byte write, and the local loads are
-                // contiguous too
+        // this group's half of the output columns of a unit's rows
+        auto out_row = [&](const FaUnit& U, int rr) -> uint4* {
+            const int R = U.row0 + rr;
+            const int tk = R / p.G, hd = U.kvh * p.G + (R - tk * p.G);
+            return reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                            (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D +
+                                            h * DH + w * (DH / 2));
+        };
+        auto zero_unit = [&](const FaUnit& U) {  // a unit without tiles: zeros
+            if (r < U.n_rows) {
+                uint4* o = out_row(U, r);
+#pragma unroll 4
+                for (int j = 0; j < DH / 16; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (U.bad && w == 0 && r == 0 && U.kvh == 0 && U.rt == 0 && h == 0)
+                report(p.err, U.bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
+        };
+        // the unit's Q rows (this CTA's head_dim part) into TMEM, once S(T_prev) (the last S
+        // MMA that reads the previous unit's Q) has completed
+        auto load_q = [&](const FaUnit& U, int T_prev) {
+            // in halves of at most 64 columns (16 x 16-byte loads in flight per thread); the
+            // first half's loads are issued before waiting for the previous unit's last S
+            constexpr int NQ = DH / 8;               // 16-byte chunks of a row's part (DH bf16)
+            constexpr int HALF = NQ > 16 ? 16 : NQ;  // chunks per round
+            const bool row_ok = r < U.n_rows_real;
+            const int R = U.row0 + (row_ok ? r : 0);
+            const int tk = R / p.G, hd = U.kvh * p.G + (R - tk * p.G);
+            const uint4* qrow = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D + h * DH);
 #pragma unroll
-                for (int c = 0; c < kTcKeys / 8; ++c)
-                    st_cluster_v4(peer_x + c * (128 * 16), pack_f16_sat(s[8 * c], s[8 * c + 1]),
-                                  pack_f16_sat(s[8 * c + 2], s[8 * c + 3]),
-                                  pack_f16_sat(s[8 * c + 4], s[8 * c + 5]),
-                                  pack_f16_sat(s[8 * c + 6], s[8 * c + 7]));
-                mbar_arrive_remote(peer_x_full);
-                if (ok) ok = mbar_wait_cluster(x_full, t & 1, p.err);
-                const uint4* xr = reinterpret_cast<const uint4*>(sX) + r;
+            for (int hf = 0; hf < NQ / HALF; ++hf) {
+                uint4 qv[HALF];
 #pragma unroll
-                for (int e = 0; e < kTcKeys / 8; ++e) {
-                    const uint4 x = xr[e * 128];
-                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = unpack_f16(w[i]);
-                        s[8 * e + 2 * i] += f.x;
-                        s[8 * e + 2 * i + 1] += f.y;
-                    }
+                for (int j = 0; j < HALF; ++j)
+                    qv[j] = row_ok ? __ldg(qrow + hf * HALF + j) : make_uint4(0u, 0u, 0u, 0u);
+                if (hf == 0) {
+                    if (T_prev >= 0 && ok) ok = mbar_wait(&step_done[T_prev % kFaSteps], (T_prev / kFaSteps) & 1, p.err);
+                    tc_fence_after();
                 }
-                mbar_arrive_remote(peer_x_free);
-            }
-
-            // scores stay raw; scale > 0, so max(raw) * scale_log2 is the max of scaled scores.
-            // With a soft-cap they are first mapped to c * tanh(scale * raw / c) in log2 units
-            // (before the mask, so masked keys stay -inf).
-            float sl2 = p.scale_log2;
-            if (SOFTCAP) {
 #pragma unroll
-                for (int e = 0; e < kTcKeys; ++e) s[e] = p.cap_log2 * tanhf(s[e] * p.cap_inner);
-                sl2 = 1.f;
-            }
-            const int kt0 = k_begin + t * kTcKeys;
-            const bool full = kt0 >= lo && kt0 + kTcKeys <= hi;
-            if (!full) {
-#pragma unroll
-                for (int e = 0; e < kTcKeys; ++e) {
-                    const int key = kt0 + e;
-                    if (key < lo || key >= hi) s[e] = -INFINITY;
-                }
-            }
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = s[i];
-#pragma unroll
-            for (int e = 8; e < kTcKeys; e += 8)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[e + i]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                             sl2;
-            const bool need = mx > m_ref + kLazyRescaleLog2;
-            const float m_new = need ? mx : m_ref;
-            if (t > 0 && ok) ok = mbar_wait(o_done, (t - 1) & 1, p.err);
-            if (t > 0 && __any_sync(0xffffffffu, need)) {
-                const float alpha = need ? exp2f(m_ref - m_new) : 1.f;
-                tc_fence_after();
-#pragma unroll 1
-                for (int j = 0; j < DH / 32; ++j) {
+                for (int j = 0; j < HALF / 8; ++j) {
                     uint32_t v[32];
-                    tmem_ld32(tO + lane_off + j * 32, v);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(tO + lane_off + j * 32, v);
-                }
-                tmem_st_wait();
-                l *= alpha;
-            }
-            m_ref = m_new;
-            // p = 2^(raw * scale_log2 - m): one FFMA and one MUFU exp2 per score
-            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k0 = kb * 64 + c * 8 + 2 * e;
-                        const float p0 = fast_exp2(fmaf(s[k0], sl2, neg_m));
-                        const float p1 = fast_exp2(fmaf(s[k0 + 1], sl2, neg_m));
-                        sum4[e] += p0 + p1;
-                        w[e] = pack_bf16(p0, p1);
+                    for (int e = 0; e < 8; ++e) {
+                        v[4 * e + 0] = qv[8 * j + e].x;
+                        v[4 * e + 1] = qv[8 * j + e].y;
+                        v[4 * e + 2] = qv[8 * j + e].z;
+                        v[4 * e + 3] = qv[8 * j + e].w;
                     }
-                    *reinterpret_cast<uint4*>(sP + kb * (kTcKeys * 128) + r * 128 +
-                                              ((c ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    tmem_st32(tQ + lane_off + (hf * HALF / 8 + j) * 32, v);
                 }
-            l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-            fence_proxy_async_smem();
+            }
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-        }
+            if (lane == 0) mbar_arrive(q_ready);
+        };
+        // finds the next unit with tiles (writing zeros for units without), or returns false
+        int u = worker - fp.n_workers;
+        auto next_tiled = [&](FaUnit& U) -> bool {
+            for (;;) {
+                u += fp.n_workers;
+                if (u >= fp.n_units) return false;
+                U = fa_unit(fp, u);
+                if (U.n_tiles > 0) return true;
+                zero_unit(U);
+            }
+        };
 
-        // epilogue: O / l -> bf16 (zeros for a sequence with a bad length)
-        if (n_tiles > 0 && ok) ok = mbar_wait(o_done, (n_tiles - 1) & 1, p.err);
-        tc_fence_after();
-        {
-            // every lane runs the collective TMEM loads; only rows of the tile store
-            const int R = row0 + (r < n_rows ? r : 0);
-            const int tk = R / p.G, hd = kvh * p.G + (R - tk * p.G);
-            uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                                   (((size_t)b * p.n_tok + tk) * p.n_q + hd) * (size_t)D +
-                                                   h * DH);
-            const float inv = (bad || l == 0.f) ? 0.f : 1.f / l;
+        FaUnit cur;
+        if (next_tiled(cur)) {
+            int T_base = 0, ord = 0;
+            float m_w = -INFINITY, l_w = 0.f;  // this group's share of l, relative to m_w
+            if (w == 0) load_q(cur, -1);
+            for (;;) {
+                const int lo_pos = cur.len - cur.n_real;  // position of the unit's token 0
+                int lo = 1, hi = 0;
+                if (r < cur.n_rows_real) {
+                    const int pos = lo_pos + (cur.row0 + r) / p.G;
+                    lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
+                    hi = pos + 1;
+                }
+                const int t0 = ((T_base & 1) == w) ? 0 : 1;
+                for (int t = t0; t < cur.n_tiles; t += 2) {
+                    const int T = T_base + t;
+                    const int buf = T & 1;  // == w
+                    // ---- S(T) from TMEM (its step has also completed P V(T-2), so P buffer
+                    // T % 2 is free) ----
+                    if (ok) ok = mbar_wait(&step_done[T % kFaSteps], (T / kFaSteps) & 1, p.err);
+                    tc_fence_after();
+                    float s[kFaKeys];
+                    {
+                        uint32_t v0[32], v1[32];
+                        const uint32_t tS = tmem + Lay::S_COL + 64 * buf + lane_off;
+                        tmem_ld32(tS, v0);
+                        tmem_ld32(tS + 32, v1);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            s[e] = __uint_as_float(v0[e]);
+                            s[32 + e] = __uint_as_float(v1[e]);
+                        }
+                    }
+
+                    if (CL > 1) {
+                        // send this row's partial scores to the peer (asynchronous stores that
+                        // count bytes on the peer's x_full), then add the peer's partial
+                        const int k = T >> 1;
+                        if (r == 0) mbar_arrive_expect_tx(&x_full[w], 128 * kFaKeys * 2);
+                        if (k >= 1 && ok) ok = mbar_wait_cluster(&x_free[w], (k - 1) & 1, p.err);
+                        // chunk-major layout X[c][r] (16-byte chunks of 8 fp16 scores): a
+                        // warp's 32 stores of chunk c are one contiguous 512-byte write
+#pragma unroll
+                        for (int c = 0; c < kFaKeys / 8; ++c)
+                            st_async_v4(peer_x + c * (128 * 16), pack_f16_sat(s[8 * c], s[8 * c + 1]),
+                                        pack_f16_sat(s[8 * c + 2], s[8 * c + 3]),
+                                        pack_f16_sat(s[8 * c + 4], s[8 * c + 5]),
+                                        pack_f16_sat(s[8 * c + 6], s[8 * c + 7]), peer_x_full);
+                        if (ok) ok = mbar_wait_cluster(&x_full[w], k & 1, p.err);
+                        const uint4* xr = reinterpret_cast<const uint4*>(sX + w * Lay::X_TILE) + r;
+#pragma unroll
+                        for (int c = 0; c < kFaKeys / 8; ++c) {
+                            const uint4 x = xr[c * 128];
+                            const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 f = unpack_f16(wd[i]);
+                                s[8 * c + 2 * i] += f.x;
+                                s[8 * c + 2 * i + 1] += f.y;
+                            }
+                        }
+                        // every lane has consumed its loads of X[w] (the adds above): the peer may
+                        // overwrite it
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote_relaxed(peer_x_free);
+                    }
+
+                    // scores stay raw; scale > 0, so max(raw) * scale_log2 is the max of the
+                    // scaled scores. With a soft-cap they are first mapped to c * tanh(scale *
+                    // raw / c) in log2 units (before the mask, so masked keys stay -inf), with
+                    // tanh(x) = 1 - 2 / (e^(2x) + 1).
+                    float sl2 = p.scale_log2;
+                    if (SOFTCAP) {
+                        const float k2 = 2.8853900817779268f * p.cap_inner;  // 2 log2(e) s / c
+                        const float c2 = 2.f * p.cap_log2;
+#pragma unroll
+                        for (int e = 0; e < kFaKeys; ++e)
+                            s[e] = fmaf(-c2, fast_rcp(fast_exp2(s[e] * k2) + 1.f), p.cap_log2);
+                        sl2 = 1.f;
+                    }
+                    const int kt0 = cur.k_begin + t * kFaKeys;
+                    if (!(kt0 >= lo && kt0 + kFaKeys <= hi)) {
+#pragma unroll
+                        for (int e = 0; e < kFaKeys; ++e) {
+                            const int key = kt0 + e;
+                            if (key < lo || key >= hi) s[e] = -INFINITY;
+                        }
+                    }
+                    float mx8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+                    for (int e = 8; e < kFaKeys; e += 8)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[e + i]);
+                    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                                     sl2;
+
+                    // ---- the row's reference after tile T-1, then after tile T ----
+                    if (T > 0 && ok) ok = mbar_wait(m_ready, (T - 1) & 1, p.err);
+                    const float m_prev = t > 0 ? mref[r] : -INFINITY;
+                    const float m_new = mx > m_prev + kLazyRescaleLog2 ? mx : m_prev;
+                    mref[r] = m_new;
+                    mbar_arrive(m_ready);
+                    if (m_new != m_w) {  // references only grow; l_w follows
+                        l_w = m_w == -INFINITY ? 0.f : l_w * exp2f(m_w - m_new);
+                        m_w = m_new;
+                    }
+                    // ---- O rows whose reference moved: rescale after P V(T-1) ----
+                    // (a row whose earlier keys were all masked has O = 0: nothing to rescale)
+                    const bool resc = t > 0 && m_new != m_prev && m_prev != -INFINITY;
+                    if (__any_sync(0xffffffffu, resc)) {
+                        // P V(T-1) completes in step T + 1
+                        if (ok) ok = mbar_wait(&step_done[(T + 1) % kFaSteps], ((T + 1) / kFaSteps) & 1, p.err);
+                        tc_fence_after();
+                        const float alpha = resc ? exp2f(m_prev - m_new) : 1.f;
 #pragma unroll 1
-            for (int j = 0; j < DH / 32; ++j) {
-                uint32_t v[32];
-                if (n_tiles > 0) {
-                    tmem_ld32(tO + lane_off + j * 32, v);
-                    tmem_ld_wait();
-                } else {
+                        for (int j = 0; j < DH / 32; ++j) {
+                            uint32_t v[32];
+                            tmem_ld32(tO + lane_off + j * 32, v);
+                            tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
-                }
-                if (r < n_rows) {
+                            for (int e = 0; e < 32; ++e)
+                                v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            tmem_st32(tO + lane_off + j * 32, v);
+                        }
+                        tmem_st_wait();
+                    }
+                    // ---- P(T) = 2^(s * scale_log2 - m) into shared memory buffer T % 2 ----
+                    const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
+                    float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t pw[kFaKeys / 2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        orow[j * 4 + e] = make_uint4(
-                            pack_bf16(__uint_as_float(v[8 * e + 0]) * inv, __uint_as_float(v[8 * e + 1]) * inv),
-                            pack_bf16(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv),
-                            pack_bf16(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv),
-                            pack_bf16(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv));
+                    for (int k2 = 0; k2 < kFaKeys / 2; ++k2) {
+                        const float p0 = fast_exp2(fmaf(s[2 * k2], sl2, neg_m));
+                        const float p1 = fast_exp2(fmaf(s[2 * k2 + 1], sl2, neg_m));
+                        sum4[k2 & 3] += p0 + p1;
+                        pw[k2] = pack_bf16(p0, p1);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(sPw + r * 128 + ((c ^ (r & 7)) * 16)) =
+                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                    l_w += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&step_ready[(T + 2) % kFaSteps]);  // P V(T) in step T + 2
                 }
+
+                // ---- next unit: its first tile's group loads its Q before this epilogue ----
+                FaUnit nxt;
+                const bool more = next_tiled(nxt);
+                const int T_next = T_base + cur.n_tiles;
+                if (more && (T_next & 1) == w) load_q(nxt, T_next - 1);
+
+                // ---- epilogue: O / l -> bf16 for this group's half of the columns ----
+                if (ok) ok = mbar_wait(o_full, ord & 1, p.err);
+                tc_fence_after();
+                {
+                    // (m, l) of both groups through the first P buffer, free once the unit's
+                    // last P V has completed (and until the next unit's first P is written)
+                    float2* ml = reinterpret_cast<float2*>(sP);
+                    ml[w * 128 + r] = make_float2(m_w, l_w);
+                    named_bar_sync(1, 256);
+                    const float2 o2 = ml[(w ^ 1) * 128 + r];
+                    named_bar_sync(1, 256);
+                    const float mf = fmaxf(m_w, o2.x);
+                    float lt = 0.f;
+                    if (m_w != -INFINITY) lt += l_w * exp2f(m_w - mf);
+                    if (o2.x != -INFINITY) lt += o2.y * exp2f(o2.x - mf);
+                    const float inv = (cur.bad || lt == 0.f) ? 0.f : 1.f / lt;
+                    // O / l in slices of up to 64 columns: each thread converts its row's slice
+                    // to bf16 in this group's P buffer (free until its next P: the unit's last P
+                    // V has completed), then each warp writes its 32 rows' slices with whole
+                    // 128-byte lines per row (rows are 2 * D bytes apart in `out`)
+                    constexpr int SW = DH / 2 < 64 ? DH / 2 : 64;  // columns per slice
+                    constexpr int CPR = SW / 8;                    // 16-byte chunks per row
+                    uint8_t* stage = sPw;
+                    const int wrow0 = (warp & 3) * 32;             // this warp's rows
+#pragma unroll 1
+                    for (int sl = 0; sl < (DH / 2) / SW; ++sl) {
+#pragma unroll
+                        for (int j = 0; j < SW / 32; ++j) {
+                            uint32_t v[32];
+                            tmem_ld32(tO + lane_off + w * (DH / 2) + sl * SW + j * 32, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = j * 4 + e;
+                                *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) * 16)) = make_uint4(
+                                    pack_bf16(__uint_as_float(v[8 * e + 0]) * inv, __uint_as_float(v[8 * e + 1]) * inv),
+                                    pack_bf16(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv),
+                                    pack_bf16(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv),
+                                    pack_bf16(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv));
+                            }
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int it2 = 0; it2 < CPR; ++it2) {
+                            const int idx = it2 * 32 + lane;
+                            const int rr = wrow0 + idx / CPR, c = idx % CPR;
+                            const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((c ^ (rr & 7)) * 16));
+                            if (rr < cur.n_rows) out_row(cur, rr)[sl * CPR + c] = val;
+                        }
+                        __syncwarp();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
+                m_w = -INFINITY;
+                l_w = 0.f;
+                if (!more) break;
+                cur = nxt;
+                T_base = T_next;
+                ++ord;
             }
         }
-        if (bad && r == 0 && kvh == 0 && rt == 0 && h == 0)
-            report(p.err, bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
     }
     tc_fence_before();
     __syncthreads();
     if (CL > 1) cluster_sync();  // the peer no longer writes into this CTA's shared memory
-    if (warp == 5) {
+    if (warp == kFaMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -562,42 +804,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ---------------------------------------------------------------------------------------------
 template <int D, int CL>
 static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
-    using Lay = TcLayout<D, CL>;
+    using Lay = FaLayout<D, CL>;
     CUtensorMap km, vm;
     // [rows][slots][D]: rows = sequences x KV heads (pages x KV heads for a paged pool)
     const uint64_t map_slots = p.page_size ? (uint64_t)p.page_size : (uint64_t)p.cap;
     const uint64_t map_rows = p.page_size ? (uint64_t)p.n_pages * p.n_kv : (uint64_t)batch * p.n_kv;
     const uint64_t dims[3] = {(uint64_t)D, map_slots, map_rows};
     const uint64_t strides[2] = {(uint64_t)D * 2, map_slots * D * 2};
-    const uint32_t box[3] = {64, (uint32_t)kTcKeys, 1};
+    const uint32_t box[3] = {64, (uint32_t)kFaKeys, 1};
     if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    TcParams tp;
-    tp.p = p;
-    const int fixed = Lay::P_BYTES + Lay::X_BYTES + 256 + 1024;  // P, X, barriers, alignment
-    int ns = (kTcSmemLimit - fixed) / Lay::SLOT;
-    if (ns > kTcMaxSlots) ns = kTcMaxSlots;
-    if (ns < 2) return cudaErrorInvalidValue;
-    tp.n_slots = ns;
+    const int fixed = Lay::FIXED + 1024;  // + alignment slack of the dynamic buffer
+    int ns = (kFaSmemLimit - fixed) / Lay::SLOT;
+    if (ns > kFaMaxSlots) ns = kFaMaxSlots;
+    if (ns < 3) return cudaErrorInvalidValue;
     const size_t smem = (size_t)ns * Lay::SLOT + fixed;
-    static int configured[64] = {0};
+
+    // per device: the shared-memory attribute, and how many CTAs (clusters) fit at once
+    static std::atomic<int> workers[64];
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemLimit);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemLimit);
-        if (e != cudaSuccess) return e;
-        configured[dev] = 1;
-    }
-    const int rows = p.n_tok * p.G;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    int n_workers = dev >= 0 && dev < 64 ? workers[dev].load(std::memory_order_relaxed) : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CL * ((rows + 127) / 128), p.n_kv, batch);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
@@ -605,10 +833,43 @@ static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
     attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(kFaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, true>, km, vm, tp)
-                           : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, false>, km, vm, tp);
+    if (n_workers <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kFaSmemLimit);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kFaSmemLimit);
+        if (e != cudaSuccess) return e;
+        int n_sm = 0;
+        e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        n_workers = n_sm / CL;
+        if (CL > 1) {
+            cudaLaunchConfig_t occ = cfg;
+            occ.gridDim = dim3(CL * n_workers);
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, prefill_tc_kernel<D, CL, false>, &occ);
+            if (e != cudaSuccess) return e;
+            if (clusters < 1) return cudaErrorInvalidConfiguration;
+            if (clusters < n_workers) n_workers = clusters;
+        }
+        if (dev >= 0 && dev < 64) workers[dev].store(n_workers, std::memory_order_relaxed);
+    }
+    FaParams fp;
+    fp.p = p;
+    fp.n_slots = ns;
+    fp.batch = batch;
+    fp.n_rt = (p.n_tok * p.G + 127) / 128;
+    fp.n_units = fp.n_rt * batch * p.n_kv;
+    fp.n_workers = fp.n_units < n_workers ? fp.n_units : n_workers;
+    cfg.gridDim = dim3(CL * fp.n_workers);
+    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, true>, km, vm, fp)
+                           : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, false>, km, vm, fp);
 }
 
 bool prefill_tc_supported(int head_dim) {
