@@ -156,6 +156,18 @@ GEMMA_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* er
         }
     }
 }
+// Non-blocking check of a phase's completion (cheaper than try_wait when it has completed).
+GEMMA_DEVINL bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Adds `bytes` to the transaction count the current phase of `bar` waits for.
 GEMMA_DEVINL void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
@@ -457,7 +469,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                     h2.slot = ps;
                     if (++ps == NS) ps = 0;
                 }
-                if (ok) ok = mbar_wait(&step_ready[i % kFaSteps], (i / kFaSteps) & 1, p.err);
+                if (ok && !mbar_test_wait(&step_ready[i % kFaSteps], (i / kFaSteps) & 1))
+                    ok = mbar_wait(&step_ready[i % kFaSteps], (i / kFaSteps) & 1, p.err);
                 if (p.k_eq_v) {
                     if (cur.valid) zero_edges(cur.slot, cur);  // the slot also serves as V
                 } else if (h2.valid) {
@@ -582,6 +595,23 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                     const int pos = lo_pos + (cur.row0 + r) / p.G;
                     lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
                     hi = pos + 1;
+                }
+                // the next unit's Q rows towards L2 while this unit runs (its loader group)
+                if (cur.n_tiles > 2) {
+                    const int u2 = u + fp.n_workers;
+                    if (u2 < fp.n_units && (((T_base + cur.n_tiles) & 1) == w)) {
+                        const FaUnit U2 = fa_unit(fp, u2);
+                        if (r < U2.n_rows_real) {
+                            const int R = U2.row0 + r;
+                            const int tk = R / p.G, hd = U2.kvh * p.G + (R - tk * p.G);
+                            const char* qrow = reinterpret_cast<const char*>(
+                                reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                (((size_t)U2.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D + h * DH);
+#pragma unroll
+                            for (int j = 0; j < (DH * 2) / 128; ++j)
+                                asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + j * 128));
+                        }
+                    }
                 }
                 const int t0 = ((T_base & 1) == w) ? 0 : 1;
                 for (int t = t0; t < cur.n_tiles; t += 2) {
