@@ -140,14 +140,15 @@ int gemma_attn_decode(void* out, const void* q, const void* const* k_cache,
  * have no counterpart: this entry point exists for callers of this library that cannot
  * allocate device memory (code running inside an allocator or memory-pool callback, a plugin
  * whose host owns every device allocation, or a latency-critical path that must not call the
- * driver's allocator). Its split scratch is a fixed 64 MiB array compiled into the library,
+ * driver's allocator). Its split scratch is a fixed 32 MiB array compiled into the library,
  * held by every GPU that loads the library until the process exits. It allocates nothing.
  *  - Arguments and results are those of gemma_attn_decode minus workspace/workspace_bytes,
  *    with the same statuses in the same order of checks: an unsupported shape gives
  *    GEMMA_ERR_UNSUPPORTED, a bad argument GEMMA_ERR_INVALID_ARG or GEMMA_ERR_CAPACITY.
  *  - Returns GEMMA_ERR_WORKSPACE, with no launch, when the arguments are valid but
- *    gemma_attn_workspace_size(...) for them is larger than 64 MiB (e.g. batch 64 x 16 query
- *    heads of head_dim 512 split 19 ways needs about 40 MB and fits).
+ *    gemma_attn_workspace_size(...) for them is larger than 32 MiB (e.g. batch 64 x 16 query
+ *    heads of head_dim 512 split 19 ways needs about 40 MB and is refused; batch-1 plans need
+ *    a few MB at most, and plans of up to 8 chunks need none).
  *  - The first call in each CUDA context (per device, and again after a device reset) looks up
  *    the array's device address with that device current; make that first call before any
  *    stream capture.

@@ -74,7 +74,13 @@ struct Plan {
     int chunk;
     size_t o_bytes;   // partial outputs
     size_t ws_bytes;  // total scratch
+    int cluster;      // the chunks of a row tile merge inside their cluster (no scratch)
 };
+
+// Splits of at most this many chunks run as one thread-block cluster per (sequence, KV head)
+// and merge through distributed shared memory; plans of up to twice as many chunks are
+// coarsened to it (one launch and no scratch beat twice the CTAs plus a combine pass).
+constexpr int kMaxClusterSplit = 8;
 
 // Decode splits each (sequence, KV head) key range into chunks so that enough CTAs stream
 // the cache at once: about one chunk per SM for small problems, about eight per SM (and at
@@ -83,7 +89,7 @@ struct Plan {
 // split. Depends only on the arguments and the SM count.
 Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim, int max_seq_len,
                int n_tok, int n_sm, bool paged = false) {
-    Plan pl{1, 1 << 30, 0, 0};
+    Plan pl{1, 1 << 30, 0, 0, 0};
     if (n_tok != 1) return pl;
     const long long T = gemma::kKeyTile;
     long long n_read = kind != GEMMA_GLOBAL && window < max_seq_len ? window : max_seq_len;
@@ -104,6 +110,16 @@ Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim,
         n_split = (n_read + chunk - 1) / chunk;
     }
     if (n_split <= 1) return pl;
+    if (n_split <= 2 * kMaxClusterSplit) {
+        if (n_split > kMaxClusterSplit) {
+            chunk = round_up((n_read + kMaxClusterSplit - 1) / kMaxClusterSplit, T);
+            n_split = (n_read + chunk - 1) / chunk;
+        }
+        pl.n_split = (int)n_split;
+        pl.chunk = (int)chunk;
+        pl.cluster = 1;
+        return pl;
+    }
     pl.n_split = (int)n_split;
     pl.chunk = (int)chunk;
     const size_t rows = (size_t)batch * n_q * n_split;
@@ -161,7 +177,7 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     const int n_sm = sm_count();
     if (n_sm < 0) return GEMMA_ERR_CUDA;
     // a padded bucket is never split over keys (pad rows have no key range to merge)
-    const Plan pl = n_real ? Plan{1, 1 << 30, 0, 0}
+    Plan pl = n_real ? Plan{1, 1 << 30, 0, 0, 0}
                            : make_plan(batch, kind, window, n_q, n_kv, head_dim, max_seq_len,
                                        n_tok, n_sm, pg != nullptr);
     if (pl.ws_bytes > 0 &&
@@ -199,8 +215,15 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
     }
     p.k_eq_v = k_eq_v ? 1 : 0;
     p.max_seq_len = max_seq_len;
+    if (pl.cluster && dtype != GEMMA_BF16) {
+        // the fp32 debug path does not split a clustered plan: one pass per row
+        pl.n_split = 1;
+        pl.chunk = 1 << 30;
+        pl.cluster = 0;
+    }
     p.n_split = pl.n_split;
     p.chunk = pl.chunk;
+    p.cluster = pl.cluster;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.softcap = softcap;
@@ -221,7 +244,7 @@ int attention(void* out, const void* q, const void* const* k_cache, const void* 
         e = gemma::launch_rows_f32(p, head_dim, dim3((unsigned)(tiles * pl.n_split), n_kv, batch),
                                    s);
     }
-    if (e == cudaSuccess && pl.n_split > 1)
+    if (e == cudaSuccess && pl.n_split > 1 && !pl.cluster)
         e = gemma::launch_combine(p, head_dim, batch, dtype == GEMMA_FP32, s);
     return e == cudaSuccess ? GEMMA_OK : GEMMA_ERR_CUDA;
 }

@@ -34,6 +34,10 @@ struct RowsParams {
     const int32_t* block_table;
     int page_size, max_pages, n_pages;
     int n_split;              // key chunks per row tile (1: write `out` directly)
+    // the n_split chunks of a row tile run as one thread-block cluster and merge their partial
+    // results through distributed shared memory (no partials in global memory, no combine
+    // pass); n_split <= 8
+    int cluster;
     int chunk;                // keys per chunk (multiple of the key tile)
     int n_stages;             // smem pipeline depth (bf16 kernel)
     float scale_log2;         // softmax scale * log2(e)

@@ -26,7 +26,7 @@
 
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
 __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;

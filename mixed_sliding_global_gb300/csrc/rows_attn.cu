@@ -65,6 +65,22 @@ GEMMA_DEVINL uint32_t tile_off(int key, int d) {
                       ((((d >> 3) & 7) ^ (key & 7)) << 4) + (d & 7) * 2);
 }
 
+// distributed shared memory of a cluster: a peer's copy of a local address, loads from it, and
+// a full cluster barrier (release / acquire)
+GEMMA_DEVINL uint32_t rows_map_peer(const void* local, uint32_t peer) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(peer));
+    return r;
+}
+GEMMA_DEVINL float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+GEMMA_DEVINL void rows_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Row geometry: local row r of tile rt is global row R = rt*16 + r, token R / G, member R % G.
 struct RowInfo {
     int token, head, pos, lo;
@@ -93,7 +109,9 @@ GEMMA_DEVINL void zero_rows(const RowsParams& p, int b, int kvh, int row0, int n
     }
 }
 
-template <int D>
+// CLUSTER: the chunks of a row tile merge inside their cluster (a separate instantiation, so
+// that the other launches carry no code for it)
+template <int D, bool CLUSTER>
 __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     rows_attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const RowsParams p) {
@@ -119,12 +137,14 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     const int row0 = rt * kRowTile;
     const int n_rows = min(kRowTile, rows_total - row0);
     const bool direct = p.n_split == 1;
+    constexpr bool clustered = CLUSTER;  // the chunks merge through their cluster
     const int len = __ldg(p.seq_lens + b);
 
     if (len < p.n_tok || (!p.ring && len > p.cap) || len > p.max_seq_len) {
+        // (every CTA of a cluster reads the same sequence, so all of them leave here)
         if (split == 0) {
             if (threadIdx.x == 0) report(p.err, GEMMA_DEVERR_SEQ_LEN);
-            if (direct) zero_rows<__nv_bfloat16>(p, b, kvh, row0, n_rows, D);
+            if (direct || clustered) zero_rows<__nv_bfloat16>(p, b, kvh, row0, n_rows, D);
         }
         return;
     }
@@ -136,8 +156,10 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     const int base = (p.ring || p.page_size) ? (first.lo & ~(T - 1)) : first.lo;
     const int kb = base + split * p.chunk;
     const int ke = min(last.pos + 1, kb + p.chunk);
-    if (kb >= ke) return;  // empty chunk: the combine pass skips it
-    const int n_keys = ke - kb;
+    // an empty chunk: the combine pass skips it; in a cluster it takes part in the merge with
+    // no keys (max -inf, sum 0)
+    if (kb >= ke && !clustered) return;
+    const int n_keys = kb >= ke ? 0 : ke - kb;
     const int n_tiles = (n_keys + T - 1) / T;
     const int nops = p.k_eq_v ? 1 : 2;
     const int stage_bytes = nops * Lay::TILE;
@@ -236,6 +258,10 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
                                     &full[s]);
                 }
             }
+        }
+        if (clustered) {  // the merge's two cluster barriers (every thread of the cluster)
+            rows_cluster_sync();
+            rows_cluster_sync();
         }
         return;
     }
@@ -420,6 +446,46 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     }
     named_bar_sync(1, kConsumerWarps * 32);
 
+    if (clustered) {
+        // Each chunk's unnormalised rows go to its own shared memory (the ring is free: every
+        // tile has been consumed); after a cluster barrier, CTA c merges columns
+        // [c D / n, (c + 1) D / n) of every row over the n chunks:
+        //   M = max_k m_k,  w_k = 2^(m_k - M),  out = sum_k w_k O_k / sum_k w_k l_k
+        float* part = reinterpret_cast<float*>(ring);  // [16][D]
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = g + 8 * half;
+            if (r >= n_rows) continue;
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                const int col = warp * (D / 8) + j * 8 + 2 * tq;
+                *reinterpret_cast<float2*>(part + r * D + col) =
+                    make_float2(o[j][2 * half], o[j][2 * half + 1]);
+            }
+        }
+        rows_cluster_sync();
+        const int ns = p.n_split;
+        const int c0 = split * D / ns, nc = (split + 1) * D / ns - c0;
+        for (int idx = threadIdx.x; idx < n_rows * nc; idx += kConsumerWarps * 32) {
+            const int r = idx / nc, col = c0 + (idx - r * nc);
+            float M = -INFINITY;
+            for (int k = 0; k < ns; ++k) M = fmaxf(M, ld_cluster_f32(rows_map_peer(sM + r, k)));
+            float L = 0.f, acc = 0.f;
+            for (int k = 0; k < ns; ++k) {
+                const float mk = ld_cluster_f32(rows_map_peer(sM + r, k));
+                const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
+                L = fmaf(wk, ld_cluster_f32(rows_map_peer(sL + r, k)), L);
+                acc = fmaf(wk, ld_cluster_f32(rows_map_peer(part + r * D + col, k)), acc);
+            }
+            const RowInfo ri = row_info(p, len, kvh, row0 + r);
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(((size_t)b * p.n_tok + ri.token) * p.n_q +
+                                                     ri.head) * (size_t)D + col] =
+                __float2bfloat16_rn(acc / L);
+        }
+        rows_cluster_sync();  // peers may still read this CTA's shared memory until here
+        return;
+    }
+
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const int r = g + 8 * half;
@@ -540,26 +606,30 @@ __global__ void __launch_bounds__(kF32RowsPerCta * 32) rows_attn_f32_kernel(cons
 // split-K combine (decode): merge the per-chunk (m, l, O) of each (sequence, query head)
 //   M = max_c m_c,  w_c = 2^(m_c - M),  out = sum_c w_c O_c / sum_c w_c l_c
 // ---------------------------------------------------------------------------------------------
-// One CTA per (query head, sequence). The chunk weights w_c and their sum are computed once
-// into shared memory; then 4 groups of threads each accumulate a quarter of the chunks for
-// every column (loads unrolled, so a group keeps several L2 reads in flight), and the groups
-// are summed through shared memory.
+// One CTA per (query head, slice of head_dim, sequence): the whole row when the (head,
+// sequence) pairs already fill the GPU, 128-column slices when they do not (small batches).
+// The chunk weights w_c and their sum are computed once into shared memory; then groups of
+// threads each accumulate a share of the chunks for the slice's columns (one float4 per
+// thread, several L2 reads in flight), and the groups are summed through shared memory.
 constexpr int kCombineThreads = 256;
-constexpr int kCombineGroups = 4;
+constexpr int kCombineSlice = 128;  // columns per CTA when rows are sliced
 
 template <typename OutT>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const RowsParams p, int D) {
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const RowsParams p, int D, int n_slices) {
     pdl_launch_dependents();
     pdl_wait();  // the previous kernel on the stream has completed
     __shared__ float s_w[128];                                  // chunk weights (n_split <= 128)
-    __shared__ float s_red[kCombineGroups][kCombineThreads / kCombineGroups * 4];
+    __shared__ float4 s_red[kCombineThreads];
     __shared__ float s_inv;
-    const int head = blockIdx.x, b = blockIdx.y;
+    const int SW = D / n_slices;
+    const int head = blockIdx.x / n_slices, col0 = (blockIdx.x - head * n_slices) * SW;
+    const int b = blockIdx.y;
     const int len = __ldg(p.seq_lens + b);
-    OutT* dst = reinterpret_cast<OutT*>(p.out) + ((size_t)b * p.n_q + head) * (size_t)D;
+    OutT* dst = reinterpret_cast<OutT*>(p.out) + ((size_t)b * p.n_q + head) * (size_t)D + col0;
     const int tid = threadIdx.x;
     if (len < 1 || (!p.ring && len > p.cap) || len > p.max_seq_len) {
-        for (int c = tid; c < D; c += blockDim.x) dst[c] = OutT(0.f);
+        for (int c = tid; c < SW; c += blockDim.x) dst[c] = OutT(0.f);
         return;
     }
     int lo = p.is_sliding ? max(0, len - p.window) : 0;
@@ -588,39 +658,35 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const RowsPara
         if (tid == 0) s_inv = 1.f / L;
     }
     __syncthreads();
-    const int per_group = kCombineThreads / kCombineGroups;  // threads per chunk group
-    const int grp = tid / per_group, col4 = tid - grp * per_group;
-    for (int cb = 0; cb < D; cb += per_group * 4) {  // same trip count for every thread
-        const int col = cb + col4 * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int tpg = SW / 4;                      // threads per chunk group (one float4 each)
+    const int n_grp = kCombineThreads / tpg;     // chunk groups
+    const int grp = tid / tpg, c4 = tid - grp * tpg;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int c = grp; c < nc && col < D; c += kCombineGroups) {
-            const float w = s_w[c];
-            const float4 v = *reinterpret_cast<const float4*>(p.o_part + (base + c) * D + col);
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+    for (int c = grp; c < nc; c += n_grp) {
+        const float w = s_w[c];
+        const float4 v = *reinterpret_cast<const float4*>(p.o_part + (base + c) * D + col0 + c4 * 4);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
+    s_red[tid] = acc;
+    __syncthreads();
+    if (grp == 0) {
+        float4 t = s_red[c4];
+        for (int g2 = 1; g2 < n_grp; ++g2) {
+            const float4 u = s_red[g2 * tpg + c4];
+            t.x += u.x;
+            t.y += u.y;
+            t.z += u.z;
+            t.w += u.w;
         }
-        *reinterpret_cast<float4*>(&s_red[grp][col4 * 4]) = acc;
-        __syncthreads();
-        if (grp == 0 && col < D) {
-            float4 t = *reinterpret_cast<const float4*>(&s_red[0][col4 * 4]);
-#pragma unroll
-            for (int g2 = 1; g2 < kCombineGroups; ++g2) {
-                const float4 u = *reinterpret_cast<const float4*>(&s_red[g2][col4 * 4]);
-                t.x += u.x;
-                t.y += u.y;
-                t.z += u.z;
-                t.w += u.w;
-            }
-            const float inv = s_inv;
-            dst[col + 0] = OutT(t.x * inv);
-            dst[col + 1] = OutT(t.y * inv);
-            dst[col + 2] = OutT(t.z * inv);
-            dst[col + 3] = OutT(t.w * inv);
-        }
-        __syncthreads();
+        const float inv = s_inv;
+        dst[c4 * 4 + 0] = OutT(t.x * inv);
+        dst[c4 * 4 + 1] = OutT(t.y * inv);
+        dst[c4 * 4 + 2] = OutT(t.z * inv);
+        dst[c4 * 4 + 3] = OutT(t.w * inv);
     }
 }
 
@@ -650,15 +716,19 @@ size_t rows_bf16_smem_bytes(int head_dim, int k_eq_v, int* n_stages) {
 
 template <int D>
 static cudaError_t launch_bf16_d(const RowsParams& p, dim3 grid, size_t smem, cudaStream_t st) {
+    auto kernel = p.cluster ? rows_attn_bf16_kernel<D, true> : rows_attn_bf16_kernel<D, false>;
     // attribute set once per device (the same value every time, so concurrent first calls
     // from several host threads are harmless)
     static std::atomic<bool> configured[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
-        cudaError_t e = cudaFuncSetAttribute(rows_attn_bf16_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(rows_attn_bf16_kernel<D, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(rows_attn_bf16_kernel<D, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_relaxed);
     }
@@ -671,7 +741,24 @@ static cudaError_t launch_bf16_d(const RowsParams& p, dim3 grid, size_t smem, cu
     const uint32_t box[3] = {64, (uint32_t)kKeyTile, 1};
     if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    return launch_pdl(rows_attn_bf16_kernel<D>, grid, dim3(kRowsThreads), smem, st, km, vm, p);
+    if (!p.cluster)
+        return launch_pdl(kernel, grid, dim3(kRowsThreads), smem, st, km, vm, p);
+    // the chunks of a row tile (consecutive blockIdx.x) form one cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kRowsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.n_split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, km, vm, p);
 }
 
 cudaError_t launch_rows_bf16(const RowsParams& p, int head_dim, dim3 grid, size_t smem,
@@ -698,10 +785,18 @@ cudaError_t launch_rows_f32(const RowsParams& p, int head_dim, dim3 grid, cudaSt
 
 cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out_fp32,
                            cudaStream_t st) {
-    const dim3 grid(p.n_q, batch);
+    int n_sm = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const int n_slices = ((long long)p.n_q * batch >= 2LL * n_sm || head_dim <= kCombineSlice)
+                             ? 1
+                             : head_dim / kCombineSlice;
+    const dim3 grid(p.n_q * n_slices, batch);
     const dim3 block(kCombineThreads);
-    if (out_fp32) return launch_pdl(combine_kernel<float>, grid, block, 0, st, p, head_dim);
-    return launch_pdl(combine_kernel<__nv_bfloat16>, grid, block, 0, st, p, head_dim);
+    if (out_fp32)
+        return launch_pdl(combine_kernel<float>, grid, block, 0, st, p, head_dim, n_slices);
+    return launch_pdl(combine_kernel<__nv_bfloat16>, grid, block, 0, st, p, head_dim, n_slices);
 }
 
 }  // namespace gemma

@@ -223,8 +223,9 @@ def test_ragged_decode_full_batch_sliding_layer():
 
 def test_split_plan_of_the_benchmark_shapes():
     """The planner leaves the batch-64 sliding layers unsplit (their 512 units fill the GPU over
-    1024-key windows: no scratch, no combine) and splits the global layers and the batch-1
-    decodes over keys (scratch needed)."""
+    1024-key windows: no scratch, no combine), splits the batch-1 sliding layers into at most
+    eight chunks merged inside their cluster (no scratch), and splits the global layers over
+    keys with a combine pass (scratch needed)."""
     import mixed_sliding_global_gb300 as g
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     assert 64 * 8 >= 2 * n_sm
@@ -232,5 +233,5 @@ def test_split_plan_of_the_benchmark_shapes():
     assert g.gemma_attn_workspace_size(64, g.GEMMA_SLIDING_RING, 1024, 16, 8, 256, 16385, 1) == 0
     assert g.gemma_attn_workspace_size_paged(64, SLIDING, 1024, 16, 8, 256, 16385, 1) == 0
     assert g.gemma_attn_workspace_size(64, GLOBAL, 0, 16, 1, 512, 16385, 1) > 0
-    assert g.gemma_attn_workspace_size(1, SLIDING, 1024, 16, 8, 256, 8192, 1) > 0
+    assert g.gemma_attn_workspace_size(1, SLIDING, 1024, 16, 8, 256, 8192, 1) == 0
     assert g.gemma_attn_workspace_size(1, GLOBAL, 0, 16, 1, 512, 8192, 1) > 0

@@ -41,7 +41,7 @@ def _caches(kc, vc):
 # the kernels did not write every partial before reading it.
 @pytest.mark.parametrize("spec,calls,cap", [
     (LayerSpec(GLOBAL, 0, 16, 1, 512, True), [([3000, 5000, 777, 4100], 11), ([700], 12)], 5056),
-    (LayerSpec(SLIDING, 1024, 16, 8, 256, False), [([4000, 1500, 3000], 11), ([1100], 12)], 4032),
+    (LayerSpec(SLIDING, 8192, 16, 8, 256, False), [([9000, 8500], 11), ([5000], 12)], 9024),
 ])
 def test_static_scratch_decode_matches_workspace_decode(spec, calls, cap):
     import mixed_sliding_global_gb300 as g
@@ -73,12 +73,12 @@ def test_static_scratch_decode_matches_workspace_decode(spec, calls, cap):
 
 
 def test_static_scratch_rejects_oversized_plans():
-    """A plan whose split scratch exceeds the built-in 64 MiB is refused before any launch."""
+    """A plan whose split scratch exceeds the built-in 32 MiB is refused before any launch."""
     import mixed_sliding_global_gb300 as g
     n_q, d, cap = 16, 512, 16448
-    B = next((b for b in range(1000, 1216, 4)
-              if g.gemma_attn_workspace_size(b, GLOBAL, 0, n_q, 1, d, cap, 1) > (64 << 20)), None)
-    assert B is not None, "no batch in range needs more than 64 MiB of split scratch"
+    B = next((b for b in range(32, 129, 4)
+              if g.gemma_attn_workspace_size(b, GLOBAL, 0, n_q, 1, d, cap, 1) > (32 << 20)), None)
+    assert B is not None, "no batch in range needs more than 32 MiB of split scratch"
     q = torch.zeros(B, 1, n_q, d, dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros(8, dtype=torch.bfloat16, device="cuda")        # never read
     sl = torch.ones(B, dtype=torch.int32, device="cuda")
