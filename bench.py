@@ -2,6 +2,7 @@
 """Benchmark of the mixed sliding/global attention step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+    python bench.py --tp --workload 12b_decode      (tensor-parallel heads, one rank per GPU)
 
 A step is one pass of the hot path over every layer of the workload: append of the new K/V
 rows (owner layers), owner resolution, attention (decode: split-K partials + combine; prefill:
@@ -648,6 +649,90 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_tp(args):
+    """Tensor-parallel decode, one rank per GPU: every rank holds its head shard of each layer
+    (tp.RankStep: query heads split over the ranks, a KV head replicated where a layer has
+    fewer than the ranks) and runs append + attention of every layer on it; the ranks exchange
+    nothing inside the step. Strong scaling: the model and batch are fixed, the heads split.
+    `value` counts the bytes all ranks move (replicated KV heads once per rank that reads
+    them); `unsharded_bytes_per_step` is the same step on one GPU."""
+    import dataclasses
+    from mixed_sliding_global_gb300.tp import RankStep
+    world, rank, local = dist_setup()
+    build_library(world, local)
+    device = torch.device("cuda", local)
+    if args.workload not in ("e4b_decode", "12b_decode"):
+        raise SystemExit("--tp times the batch-1 decode workloads (e4b_decode, 12b_decode)")
+    w, _ = workload(args.workload)
+    st = DeviceState(w, 1234, device)   # the whole model's inputs: same seed on every rank
+    rs = RankStep(w.layers, w.owner_map, rank, world, device)
+    for l in range(w.n_layers):
+        if w.is_owner(l):
+            rs.load_cache(l, st.kc[l], st.vc[l])
+    loc = rs.local_inputs([(st.q[l], st.k_new[l], st.v_new[l], st.write_pos, st.seq_lens)
+                           for l in range(w.n_layers)])
+    msl = st.max_seq_len
+    del st
+    torch.cuda.empty_cache()
+    outs = [torch.empty_like(x[0]) for x in loc]
+    scales = [w.scale(l) for l in range(w.n_layers)]
+    rs.run(loc, outs, scales, msl)   # eager pass: workspaces, kernel attributes, error word
+    torch.cuda.synchronize()
+    if rs.err.item() != 0:
+        raise RuntimeError(f"device error word {rs.err.item()} in the eager pass")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rs.run(loc, outs, scales, msl)
+    for _ in range(args.warmup):
+        g.replay()
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0, t1 = make_event(False), make_event(False)
+    t0.record()
+    for _ in range(args.steps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if rs.err.item() != 0:
+        raise RuntimeError(f"device error word {rs.err.item()} after the timed region")
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
+
+    import mixed_sliding_global_gb300 as gemma
+
+    def shard_workload(r):
+        from mixed_sliding_global_gb300.tp import head_shard
+        ls = [dataclasses.replace(s, n_q=sh.n_q, n_kv=sh.n_kv) for s, sh in
+              zip(w.layers, (head_shard(s.n_q, s.n_kv, r, world) for s in w.layers))]
+        return synth.Workload(w.name, ls, w.owner_map, w.batch, w.dtype, w.n_new, w.ctx_lens,
+                              w.capacity)
+    total = sum(step_work(shard_workload(r)) for r in range(world))
+    mine = shard_workload(rank)
+    launches = 0
+    for l, s in enumerate(mine.layers):
+        launches += (1 if mine.is_owner(l) else 0) + 1
+        launches += gemma.gemma_attn_workspace_size(w.batch, s.kind, s.window, s.n_q, s.n_kv,
+                                                    s.head_dim, msl, 1) > 0
+    line = {"metric": METRIC, "mode": "tensor-parallel decode", "value":
+            total / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) drawn on the device, stored as bf16)",
+            "config": {"workload": args.workload, "batch": w.batch, "layers": w.n_layers,
+                       "ctx": max(w.ctx_lens), "parallelism": f"tp{world}",
+                       "append": "separate launch", "l2": "inputs larger than L2"},
+            "bytes_per_step_all_ranks": total, "unsharded_bytes_per_step": step_work(w),
+            "gpu_launches": launches * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_native(args):
     world, rank, local = dist_setup()
     build_library(world, local)
@@ -851,6 +936,8 @@ def main():
                          "launch (default: the append inside the attention launch)")
     ap.add_argument("--softcap", type=float, default=None,
                     help="time the workload through the soft-capped entry point with this cap")
+    ap.add_argument("--tp", action="store_true",
+                    help="batch-1 decode workloads: tensor-parallel heads, one rank per GPU")
     ap.add_argument("--quick", action="store_true",
                     help="main workload only (no e2e, CPU baseline or other configurations)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -862,6 +949,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.tp:
+        run_tp(args)
     else:
         run_native(args)
 

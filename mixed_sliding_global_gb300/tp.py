@@ -72,3 +72,106 @@ def tp_decode(out_local, q_local, k_local, v_local, owner_map, layer, seq_lens, 
     gemma_attn_decode(out_local, q_local, k_local, v_local, owner_map, layer, seq_lens,
                       max_seq_len, kind=kind, window=window, n_kv=s.n_kv, k_eq_v=k_eq_v,
                       scale=scale, workspace=workspace, device_error=device_error, stream=stream)
+
+
+class RankStep:
+    """One rank's share of a decode step over every layer of a model (one process per GPU).
+
+    The rank holds its head shard of each owner layer's cache on its own device (the pages'
+    "head r -> rank r", with a KV head replicated where a layer has fewer KV heads than ranks),
+    appends the step's rows of its KV heads and attends its query heads of every layer. Ranks
+    exchange nothing during the step; `gather` all-gathers the per-layer outputs along the query
+    heads afterwards (the sum over ranks of the real model follows the row-parallel output
+    projection, outside this path).
+
+    `append(step, layer, k_new, v_new, write_pos, spec)` (into step.k / step.v) and
+    `attend(step, out, q, layer, seq_lens, max_seq_len, spec, shard, scale)` default to this
+    library's calls; they are parameters so that the same rank logic runs on CPU ranks with a
+    stand-in for the kernels.
+    """
+
+    def __init__(self, layers, owner_map, rank: int, world: int, device, append=None,
+                 attend=None):
+        self.layers, self.owner_map = list(layers), list(owner_map)
+        self.rank, self.world, self.device = rank, world, device
+        self.shards = [head_shard(s.n_q, s.n_kv, rank, world) for s in self.layers]
+        self.k = [None] * len(self.layers)
+        self.v = [None] * len(self.layers)
+        self._append = append or RankStep._lib_append
+        self._attend = attend or RankStep._lib_attend
+        self.err = None
+        self._ws = {}   # per-layer split workspace, kept across steps
+
+    # ---- the library's calls on this rank's device ----
+    def _lib_append(self, layer, k_new, v_new, write_pos, spec):
+        from .binding import gemma_kv_append
+        if self.err is None:
+            self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        gemma_kv_append(self.k, self.v, self.owner_map, layer, k_new, v_new, write_pos,
+                        k_eq_v=spec.k_eq_v, device_error=self.err)
+
+    def _lib_attend(self, out, q, layer, seq_lens, max_seq_len, spec, shard, scale):
+        from .binding import gemma_attn_workspace_size
+        if self.err is None:
+            self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        ws_n = gemma_attn_workspace_size(q.shape[0], spec.kind, spec.window, shard.n_q, shard.n_kv,
+                                         spec.head_dim, max_seq_len, 1)
+        ws = self._ws.get(layer)
+        if ws is None or ws.numel() < ws_n:
+            ws = self._ws[layer] = torch.zeros(max(ws_n, 16), dtype=torch.uint8,
+                                               device=self.device)
+        tp_decode(out, q, self.k, self.v, self.owner_map, layer, seq_lens, max_seq_len, s=shard,
+                  kind=spec.kind, window=spec.window, k_eq_v=spec.k_eq_v, scale=scale,
+                  workspace=ws, device_error=self.err)
+
+    # ---- the step ----
+    def load_cache(self, layer: int, k_cache: torch.Tensor, v_cache=None) -> None:
+        """This rank's shard of an owner layer's full cache [B][n_kv][cap][d], on its device."""
+        sh = self.shards[layer]
+        self.k[layer] = shard_cache(k_cache, sh).to(self.device)
+        self.v[layer] = None if v_cache is None else shard_cache(v_cache, sh).to(self.device)
+
+    def local_inputs(self, layer_inputs):
+        """This rank's slice of every layer's inputs, on its device; layer_inputs[l] = (q, k_new,
+        v_new, write_pos, seq_lens) with the full head dimension."""
+        loc = []
+        for l, (q, k_new, v_new, write_pos, seq_lens) in enumerate(layer_inputs):
+            sh = self.shards[l]
+            own = self.owner_map[l] == l
+            loc.append((shard_q(q, sh).to(self.device),
+                        shard_new_rows(k_new, sh).to(self.device) if own else None,
+                        shard_new_rows(v_new, sh).to(self.device) if own and v_new is not None
+                        else None,
+                        write_pos.to(self.device), seq_lens.to(self.device)))
+        return loc
+
+    def run(self, local, outs, scales, max_seq_len: int) -> None:
+        """The rank's step on inputs already sliced (local_inputs): append (owner layers) and
+        attend every layer into outs[l] [B][1][n_q / world][d]. Library calls only, so the
+        step can be captured in a CUDA graph."""
+        for l, spec in enumerate(self.layers):
+            q, k_new, v_new, write_pos, seq_lens = local[l]
+            if self.owner_map[l] == l:
+                self._append(self, l, k_new, v_new, write_pos, spec)
+            self._attend(self, outs[l], q, l, seq_lens, max_seq_len, spec, self.shards[l],
+                         scales[l])
+
+    def step(self, layer_inputs, scales, max_seq_len: int):
+        """local_inputs + run; returns this rank's output of every layer."""
+        local = self.local_inputs(layer_inputs)
+        outs = [torch.empty_like(x[0]) for x in local]
+        self.run(local, outs, scales, max_seq_len)
+        return outs
+
+    def gather(self, outs, group=None):
+        """All-gather each layer's output along the query heads (rank-major), outside the
+        attention step; returns the full outputs [B][1][n_q][d] on every rank."""
+        if self.world == 1:
+            return list(outs)
+        import torch.distributed as dist
+        full = []
+        for o in outs:
+            parts = [torch.empty_like(o) for _ in range(self.world)]
+            dist.all_gather(parts, o.contiguous(), group=group)
+            full.append(torch.cat(parts, dim=2))
+        return full

@@ -103,3 +103,72 @@ def test_gloo_ranks_gather_the_unsharded_step(wname, world):
     ref = oracle_outputs(w, host_inputs(w, layers), layers)
     for l in layers:
         assert torch.equal(gathered[l], ref[l]), l
+
+
+def _driver_worker(rank, world, port, wname, out):
+    """The rank driver (tp.RankStep) on a CPU gloo rank, with the oracle standing in for the
+    kernels: shards loaded, rows appended, every layer attended, outputs all-gathered."""
+    import dataclasses
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    import synth
+    from harness import host_inputs
+    from oracle import load_oracle
+    from mixed_sliding_global_gb300.tp import RankStep
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w = {"e4b": lambda: synth.e4b_decode(ctx=300),
+         "12b": lambda: synth.b12_decode(n_layers=6, ctx=700)}[wname]()
+    layers = list(range(w.n_layers))
+    hb = host_inputs(w, layers)
+    orc = load_oracle()
+
+    def append(step, l, k_new, v_new, write_pos, spec):
+        orc.kv_append(step.k[l], k_new, write_pos.tolist())
+        if v_new is not None:
+            orc.kv_append(step.v[l], v_new, write_pos.tolist())
+
+    def attend(step, out, q, l, seq_lens, max_seq_len, spec, sh, scale):
+        local = [dataclasses.replace(s, n_q=x.n_q, n_kv=x.n_kv)
+                 for s, x in zip(w.layers, step.shards)]
+        out.copy_(orc.attention(local, w.owner_map, l, step.k, step.v, q, seq_lens.tolist(),
+                                scale))
+
+    step = RankStep(w.layers, w.owner_map, rank, world, "cpu", append=append, attend=attend)
+    for l in layers:
+        if w.is_owner(l):
+            step.load_cache(l, hb[l].k_cache, hb[l].v_cache)
+    inputs = [(hb[l].q, hb[l].k_new, hb[l].v_new, hb[l].write_pos, hb[l].seq_lens)
+              for l in layers]
+    outs = step.step(inputs, [w.scale(l) for l in layers], max(w.ctx_lens))
+    full = step.gather(outs)
+    if rank == 0:
+        out["full"] = full
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("wname,world", [("e4b", 2), ("12b", 2)])
+def test_rank_driver_on_gloo_ranks(wname, world):
+    """tp.RankStep, one process per rank: the gathered outputs equal the unsharded step's,
+    rounded to the step's dtype alike (every query head's arithmetic is the same)."""
+    import synth
+    from harness import host_inputs, oracle_outputs
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_driver_worker, args=(r, world, port, wname, out))
+                 for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=300)
+            assert p.exitcode == 0
+        gathered = out["full"]
+    w = {"e4b": lambda: synth.e4b_decode(ctx=300),
+         "12b": lambda: synth.b12_decode(n_layers=6, ctx=700)}[wname]()
+    layers = list(range(w.n_layers))
+    ref = oracle_outputs(w, host_inputs(w, layers), layers)
+    for l in layers:
+        assert torch.equal(gathered[l], ref[l].to(gathered[l].dtype)), l

@@ -52,3 +52,35 @@ def test_rank_slices_match_the_oracle(wname, world):
     assert err.item() == 0
     for l in layers:
         compare(torch.cat(outs[l], dim=2), ref[l], w.dtype)
+
+
+@pytest.mark.parametrize("wname,world", [("e4b", 1), ("e4b", 2), ("12b", 2)])
+def test_rank_driver_with_the_library(wname, world):
+    """tp.RankStep with the library's calls: each rank's step (load its shards, append, attend
+    every layer) run in turn on one GPU, outputs concatenated over the query heads in rank
+    order (what `gather` all-gathers), against the oracle's unsharded step. At world 1 the
+    driver's own gather is used."""
+    from mixed_sliding_global_gb300.tp import RankStep
+    w = {"e4b": lambda: synth.e4b_decode(ctx=900),
+         "12b": lambda: synth.b12_decode(n_layers=6, ctx=3000)}[wname]()
+    layers = list(range(w.n_layers))
+    hb = host_inputs(w, layers)
+    ref = oracle_outputs(w, hb, layers)
+    inputs = [(hb[l].q, hb[l].k_new, hb[l].v_new, hb[l].write_pos, hb[l].seq_lens)
+              for l in layers]
+    scales = [w.scale(l) for l in layers]
+    parts = {l: [] for l in layers}
+    for rank in range(world):
+        rs = RankStep(w.layers, w.owner_map, rank, world, "cuda")
+        for l in layers:
+            if w.is_owner(l):
+                rs.load_cache(l, hb[l].k_cache, hb[l].v_cache)
+        outs = rs.step(inputs, scales, max(w.ctx_lens))
+        if world == 1:
+            outs = rs.gather(outs)
+        torch.cuda.synchronize()
+        assert rs.err.item() == 0
+        for l in layers:
+            parts[l].append(outs[l])
+    for l in layers:
+        compare(torch.cat(parts[l], dim=2).cpu(), ref[l], w.dtype)
