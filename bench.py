@@ -430,7 +430,10 @@ def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rot
                     softcap=None, n_real=None, fused=False, ring=None, paged=None):
     """Capture one graph per step (rotating over `rotations` independent input copies) and
     time `steps` replays after `warmup` replays. Returns step time and, with per_launch, the
-    mean duration of each layer's attention launch over the timed replays."""
+    mean duration of each layer's attention launch, taken in a second pass of `steps` replays
+    of graphs with an event pair around every launch (event nodes cost a few microseconds
+    each and break the overlap of consecutive launches, so the step time is taken without
+    them)."""
     states = [DeviceState(w, 1234 + 17 * r, device, phys, softcap, n_real, fused, ring, paged)
               for r in range(rotations)]
     for st in states:   # eager pass: sets kernel attributes, checks the error word
@@ -439,14 +442,7 @@ def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rot
     for st in states:
         if st.err.item() != 0:
             raise RuntimeError(f"device error word {st.err.item()} in the eager pass")
-    ev = []
-    graphs = []
-    for k in range(warmup + steps):
-        e = None
-        if per_launch and k >= warmup:
-            e = [(make_event(True), make_event(True)) for _ in range(w.n_layers)]
-        ev.append(e)
-        graphs.append(capture(states[k % rotations], e))
+    graphs = [capture(states[k % rotations]) for k in range(warmup + steps)]
     torch.cuda.synchronize()
     for k in range(warmup):
         graphs[k].replay()
@@ -463,16 +459,27 @@ def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rot
     barrier(world)
     clk = clocks.stop()
     ms = t0.elapsed_time(t1) / steps
+    del graphs
     launch_ms = None
     if per_launch:
-        launch_ms = [sum(ev[k][l][0].elapsed_time(ev[k][l][1]) for k in range(warmup, warmup + steps))
-                     / steps for l in range(w.n_layers)]
+        ev = [[(make_event(True), make_event(True)) for _ in range(w.n_layers)]
+              for _ in range(steps)]
+        eg = [capture(states[k % rotations], ev[k]) for k in range(steps)]
+        for k in range(min(warmup, steps)):
+            eg[k].replay()
+        torch.cuda.synchronize()
+        for k in range(steps):
+            eg[k].replay()
+        torch.cuda.synchronize()
+        launch_ms = [sum(ev[k][l][0].elapsed_time(ev[k][l][1]) for k in range(steps)) / steps
+                     for l in range(w.n_layers)]
+        del eg
     for st in states:
         if st.err.item() != 0:
             raise RuntimeError(f"device error word {st.err.item()} after the timed region")
     info = {"launches_per_step": states[0].launches_per_step(),
             "cache_bytes": sum(s.cache_bytes for s in states)}
-    del graphs, states
+    del states
     torch.cuda.empty_cache()
     return ms, launch_ms, clk, info
 
@@ -647,6 +654,32 @@ def run_reference(args):
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def run_logits(args):
+    """The greedy step after the LM head alone (final-logit soft-cap + argmax of [64][262144]
+    bf16 logits), one JSON line; the default run reports it under `also`."""
+    world, rank, local = dist_setup()
+    build_library(world, local)
+    device = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    ms, nbytes, launches, clk = logit_run(args.steps, args.warmup, device, world)
+    ms = max_over_ranks(ms, world)
+    v = world * nbytes / (ms * 1e-3) / 1e9
+    line = {"metric": "logit soft-cap + argmax HBM GB/s", "value": v, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": "logits", "batch": 64,
+                                            "vocab": synth.VOCAB, "softcap": synth.LOGIT_SOFTCAP},
+            "roofline": {"bound": "hbm", "achieved": v / world, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": v / world / peaks["hbm_gbs"],
+                         "bytes_per_call": nbytes, "peak_source": peak_src},
+            "gpu_launches": launches * 4 * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 def run_tp(args):
@@ -922,7 +955,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="ragged_decode",
-                    choices=["ragged_decode", "e4b_decode", "12b_decode", "prefill"])
+                    choices=["ragged_decode", "e4b_decode", "12b_decode", "prefill", "logits"])
     ap.add_argument("--batch", type=int, default=None,
                     help="smaller ragged batch (profiling captures only; not a bench line)")
     ap.add_argument("--layers", type=int, default=None,
@@ -949,6 +982,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "logits":
+        run_logits(args)
     elif args.tp:
         run_tp(args)
     else:

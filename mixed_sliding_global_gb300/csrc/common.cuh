@@ -83,6 +83,49 @@ GEMMA_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
     }
 }
 
+// Waits with cluster-scope acquire (data that another CTA of the cluster wrote, or sent with
+// st.async, becomes visible).
+GEMMA_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (data written by the peer CTA becomes visible).
+GEMMA_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* err) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+            report(err, GEMMA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+// Asynchronous stores into a CTA of the cluster (shared::cluster address), completing bytes
+// on that CTA's mbarrier.
+GEMMA_DEVINL void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                              uint32_t mbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+            "r"(addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(mbar)
+        : "memory");
+}
+GEMMA_DEVINL void st_async_v2(uint32_t addr, float a, float b, uint32_t mbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+            addr),
+        "f"(a), "f"(b), "r"(mbar)
+        : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // bulk asynchronous copies (TMA, non-tensor form): global -> shared, completion on mbarrier
 // ---------------------------------------------------------------------------------------------
@@ -121,6 +164,9 @@ GEMMA_DEVINL void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
 
 GEMMA_DEVINL void named_bar_sync(int id, int n_threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
+}
+GEMMA_DEVINL void named_bar_arrive(int id, int n_threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
 }
 
 GEMMA_DEVINL float warp_max(float v) {

@@ -107,14 +107,6 @@ GEMMA_DEVINL uint32_t map_to_peer(const void* local, uint32_t peer) {
 }
 // Asynchronous 16-byte store into the peer CTA's shared memory; its completion counts 16 bytes
 // of transactions on the peer's mbarrier `mbar` (both cluster shared-memory addresses).
-GEMMA_DEVINL void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                              uint32_t mbar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
-            "r"(addr),
-        "r"(a), "r"(b), "r"(c), "r"(d), "r"(mbar)
-        : "memory");
-}
 // two fp32 -> packed fp16 (lo in the low half), round to nearest; values beyond the fp16
 // range saturate to +-65504 instead of becoming infinite
 GEMMA_DEVINL uint32_t pack_f16_sat(float lo, float hi) {
@@ -132,29 +124,6 @@ GEMMA_DEVINL float2 unpack_f16(uint32_t v) {
 GEMMA_DEVINL void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
-}
-GEMMA_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait with cluster-scope acquire (data written by the peer CTA becomes visible).
-GEMMA_DEVINL bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* err) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
-            report(err, GEMMA_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
 }
 // Non-blocking check of a phase's completion (cheaper than try_wait when it has completed).
 GEMMA_DEVINL bool mbar_test_wait(uint64_t* bar, uint32_t parity) {

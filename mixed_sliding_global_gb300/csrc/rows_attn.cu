@@ -19,7 +19,13 @@
 //  - eight consumer warps: (1) S = Q K^T with mma.sync m16n8k16 (warps split keys x head_dim),
 //    (2) per-row online softmax in exp2 form with warp shuffles, P rounded to bf16,
 //    (3) O = diag(alpha) O + P V (warps split head_dim);
-//  - fp32 accumulation throughout; partial (m, l, O) per chunk when the keys are split.
+//  - the producer warp starts its loads as soon as the grid may read memory, while the consumer
+//    warps stage the Q rows in the ring's last stage and take their Q fragments into registers
+//    (the stage is then released to the producer);
+//  - fp32 accumulation throughout; partial (m, l, O) per chunk when the keys are split: merged by
+//    combine_kernel, or, when a row tile's chunks form one thread-block cluster (at most 8),
+//    inside the launch: each chunk sends every CTA of the cluster its part of that CTA's column
+//    slice through distributed shared memory (st.async), and each CTA merges its slice.
 #include <atomic>
 
 #include "attn_internal.h"
@@ -43,18 +49,18 @@ constexpr float kLazyRescaleLog2 = 8.f;  // move the softmax reference only past
 
 template <int D>
 struct RowsLayout {
-    static constexpr int ROW = 2 * D + 16;      // padded bytes per Q row in shared memory
+    static constexpr int ROW = 2 * D + 16;      // padded bytes per Q row (staged in the ring)
     static constexpr int BOX = kKeyTile * 128;  // one TMA box: 32 keys x 64 columns (swizzled)
     static constexpr int TILE = (D / 64) * BOX; // one K or V tile
     static constexpr int KSPLIT = D >= 512 ? 4 : 2;  // warps sharing one n-tile in S = QK^T
     static constexpr int S_STRIDE = kKeyTile + 8;    // fp32 words per S row
     static constexpr int P_STRIDE = kKeyTile + 8;    // bf16 elements per P row
-    static constexpr int Q_OFF = 0;
-    static constexpr int S_OFF = Q_OFF + kRowTile * ROW;
+    static constexpr int S_OFF = 0;
     static constexpr int P_OFF = S_OFF + KSPLIT * kRowTile * S_STRIDE * 4;
     static constexpr int STAT_OFF = P_OFF + kRowTile * P_STRIDE * 2;  // alpha, m, l [16] each
     static constexpr int BAR_OFF = (STAT_OFF + 3 * kRowTile * 4 + 15) / 16 * 16;
-    static constexpr int RING_OFF = (BAR_OFF + 2 * kMaxStages * 8 + 1023) / 1024 * 1024;
+    // barriers: full[kMaxStages], empty[kMaxStages], recv (cluster merge)
+    static constexpr int RING_OFF = (BAR_OFF + (2 * kMaxStages + 1) * 8 + 1023) / 1024 * 1024;
 };
 
 // Byte offset of element (key, d) in a K/V tile written by TMA with 128-byte swizzle: box
@@ -80,6 +86,14 @@ GEMMA_DEVINL float ld_cluster_f32(uint32_t addr) {
 GEMMA_DEVINL void rows_cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+GEMMA_DEVINL void rows_cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+GEMMA_DEVINL void rows_cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// Column slices of the cluster merge, in column pairs: CTA c owns columns
+// [merge_col(c), merge_col(c + 1)); merge_owner(col) is the CTA whose slice holds col (even).
+GEMMA_DEVINL int merge_col(int c, int D, int ns) { return 2 * ((c * (D / 2)) / ns); }
+GEMMA_DEVINL int merge_owner(int col, int D, int ns) { return ((col / 2 + 1) * ns - 1) / (D / 2); }
 
 // Row geometry: local row r of tile rt is global row R = rt*16 + r, token R / G, member R % G.
 struct RowInfo {
@@ -116,7 +130,6 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     rows_attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const RowsParams p) {
     pdl_launch_dependents();
-    pdl_wait();  // the previous kernel on the stream has completed
     using Lay = RowsLayout<D>;
     constexpr int T = kKeyTile;
     constexpr int KSPLIT = Lay::KSPLIT;
@@ -138,6 +151,8 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     const int n_rows = min(kRowTile, rows_total - row0);
     const bool direct = p.n_split == 1;
     constexpr bool clustered = CLUSTER;  // the chunks merge through their cluster
+
+    pdl_wait();  // the previous kernel on the stream has completed
     const int len = __ldg(p.seq_lens + b);
 
     if (len < p.n_tok || (!p.ring && len > p.cap) || len > p.max_seq_len) {
@@ -165,7 +180,6 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     const int stage_bytes = nops * Lay::TILE;
     const int S = p.n_stages;
 
-    uint8_t* sQ = smem + Lay::Q_OFF;
     float* sS = reinterpret_cast<float*>(smem + Lay::S_OFF);
     __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(smem + Lay::P_OFF);
     float* sAlpha = reinterpret_cast<float*>(smem + Lay::STAT_OFF);
@@ -173,20 +187,37 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     float* sL = sM + kRowTile;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFF);
     uint64_t* empty = full + kMaxStages;
+    uint64_t* recv = full + 2 * kMaxStages;  // cluster merge: this CTA's column slice arrived
     uint8_t* ring = smem + Lay::RING_OFF;
+    // The Q rows are staged in the ring's last stage: once every consumer warp holds its Q
+    // fragments in registers it releases that stage (one extra phase of empty[S - 1]), and
+    // only then does the producer load a key tile there.
+    uint8_t* sQ = ring + (S - 1) * stage_bytes;
+    static_assert(kRowTile * Lay::ROW <= Lay::TILE, "Q rows fit in one ring stage");
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+    // The producer warp initialises the ring's barriers and starts its loads at once; the
+    // consumer warps meanwhile stage the Q rows, and wait for both at named barrier 2.
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            for (int s = 0; s < S; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kConsumerWarps);
+            }
+            if (clustered) mbar_init(recv, 1);
+            fence_barrier_init();
+            if (clustered) {
+                // every chunk sends this CTA its rows' slice of columns and its (m, l) pairs
+                const int c0 = merge_col(split, D, p.n_split), c1 = merge_col(split + 1, D, p.n_split);
+                mbar_arrive_expect_tx(recv, (uint32_t)(p.n_split * n_rows * ((c1 - c0) * 4 + 8)));
+            }
         }
-        fence_barrier_init();
-    }
-    // Q rows of the tile (zero beyond n_rows), P = 0, row statistics
-    {
+        __syncwarp();
+        named_bar_arrive(2, kRowsThreads);
+    } else {
+        // Q rows of the tile (zero beyond n_rows), P = 0, row statistics
         const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q);
         constexpr int CH = D / 8;
-        for (int idx = threadIdx.x; idx < kRowTile * CH; idx += blockDim.x) {
+        for (int idx = threadIdx.x; idx < kRowTile * CH; idx += kConsumerWarps * 32) {
             const int r = idx / CH, ch = idx - r * CH;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (r < n_rows) {
@@ -197,11 +228,11 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
             *reinterpret_cast<uint4*>(sQ + r * Lay::ROW + ch * 16) = v;
         }
         uint32_t* p32 = reinterpret_cast<uint32_t*>(sP);
-        for (int idx = threadIdx.x; idx < kRowTile * Lay::P_STRIDE / 2; idx += blockDim.x)
+        for (int idx = threadIdx.x; idx < kRowTile * Lay::P_STRIDE / 2; idx += kConsumerWarps * 32)
             p32[idx] = 0u;
         if (threadIdx.x < 3 * kRowTile) sAlpha[threadIdx.x] = 0.f;
+        named_bar_sync(2, kRowsThreads);
     }
-    __syncthreads();
 
     if (warp == kConsumerWarps) {
         // ---------------- producer warp: tiled TMA loads of the K/V rows in range --------------
@@ -241,7 +272,9 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
         if (lane == 0) {
             for (int t = 0; t < n_tiles; ++t) {
                 const int s = t % S;
-                if (t >= S && !mbar_wait(&empty[s], ((t / S) - 1) & 1, p.err)) break;
+                // stage S - 1 has one extra phase: the consumers' release of the Q rows
+                const int ph = t / S - (s == S - 1 ? 0 : 1);
+                if (ph >= 0 && !mbar_wait(&empty[s], ph & 1, p.err)) break;
                 uint8_t* dk = ring + s * stage_bytes;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
                 // cache row and slot of the tile's first key (a bad page index reads zeros)
@@ -261,7 +294,8 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
         }
         if (clustered) {  // the merge's two cluster barriers (every thread of the cluster)
             rows_cluster_sync();
-            rows_cluster_sync();
+            rows_cluster_arrive_release();
+            rows_cluster_wait();
         }
         return;
     }
@@ -278,6 +312,8 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
         const uint32_t addr = smem_u32(sQ + (lane & 15) * Lay::ROW + (d0 + (lane >> 4) * 8) * 2);
         ldsm_x4(addr, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[S - 1]);  // this warp's Q fragments are in registers
 
     // rows owned by this warp in the softmax step: warp and warp + 8
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
@@ -343,40 +379,82 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
         }
         named_bar_sync(1, kConsumerWarps * 32);
 
-        // (2) online softmax of rows warp and warp + 8: lane = key of the tile
+        // (2) online softmax of rows warp and warp + 8: lane = key of the tile. At head_dim 512
+        // (every row of the tile real: 16 query heads per KV head) the two rows go through each
+        // step together, so that their shuffle and exponential latencies overlap.
+        if constexpr (D >= 512) {
+            float sv[2], pe[2];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int r = warp + 8 * rr;
-            if (r < n_rows) {
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = warp + 8 * rr;
                 const int key = kb + t * T + lane;
-                const bool valid = lane < rows_valid && key >= r_lo[rr] && key < r_hi[rr];
-                float sv = 0.f;
+                const bool valid = r < n_rows && lane < rows_valid && key >= r_lo[rr] && key < r_hi[rr];
+                float acc = 0.f;
 #pragma unroll
-                for (int kq = 0; kq < KSPLIT; ++kq)
-                    sv += sS[(kq * kRowTile + r) * Lay::S_STRIDE + lane];
-                // scaled score in log2 units (soft-capped when a cap is set); masked keys -inf
-                if (!valid) sv = -INFINITY;
-                else if (p.softcap > 0.f) sv = p.cap_log2 * tanhf(sv * p.cap_inner);
-                else sv *= p.scale_log2;
-                // exponentials against the running reference maximum while the tile maximum
-                // is reduced; the reference moves (and the row is recomputed) only when the
-                // tile maximum exceeds it by more than 2^8, so the result is unchanged (the
-                // final division uses the same reference) and the common tile has no
-                // maximum -> exponential dependency. l is kept per lane (every lane's share is
-                // rescaled alike) and summed over the warp once, at the end.
-                const float m_old = m_run[rr];
-                float pe = exp2f(sv - (m_old == -INFINITY ? 0.f : m_old));
-                const float mx = warp_max(sv);
+                for (int kq = 0; kq < KSPLIT; ++kq) acc += sS[(kq * kRowTile + r) * Lay::S_STRIDE + lane];
+                if (!valid) sv[rr] = -INFINITY;
+                else if (p.softcap > 0.f) sv[rr] = p.cap_log2 * tanhf(acc * p.cap_inner);
+                else sv[rr] = acc * p.scale_log2;
+                pe[rr] = fast_exp2(sv[rr] - (m_run[rr] == -INFINITY ? 0.f : m_run[rr]));
+            }
+            float mx0 = sv[0], mx1 = sv[1];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = warp + 8 * rr;
+                const float mx = rr ? mx1 : mx0;
                 float alpha = 1.f;
-                if (mx > m_old + kLazyRescaleLog2) {  // the same decision in every lane
-                    alpha = exp2f(m_old - mx);         // 0 while the reference is -inf
+                if (mx > m_run[rr] + kLazyRescaleLog2) {  // the same decision in every lane
+                    alpha = fast_exp2(m_run[rr] - mx);   // 0 while the reference is -inf
                     m_run[rr] = mx;
-                    pe = exp2f(sv - mx);
+                    pe[rr] = fast_exp2(sv[rr] - mx);
                 }
-                const __nv_bfloat16 pb = __float2bfloat16_rn(pe);
-                sP[r * Lay::P_STRIDE + lane] = pb;
-                l_run[rr] = l_run[rr] * alpha + __bfloat162float(pb);
-                if (lane == 0) sAlpha[r] = alpha;
+                if (r < n_rows) {
+                    const __nv_bfloat16 pb = __float2bfloat16_rn(pe[rr]);
+                    sP[r * Lay::P_STRIDE + lane] = pb;
+                    l_run[rr] = l_run[rr] * alpha + __bfloat162float(pb);
+                    if (lane == 0) sAlpha[r] = alpha;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = warp + 8 * rr;
+                if (r < n_rows) {
+                    const int key = kb + t * T + lane;
+                    const bool valid = lane < rows_valid && key >= r_lo[rr] && key < r_hi[rr];
+                    float sv = 0.f;
+#pragma unroll
+                    for (int kq = 0; kq < KSPLIT; ++kq)
+                        sv += sS[(kq * kRowTile + r) * Lay::S_STRIDE + lane];
+                    // scaled score in log2 units (soft-capped when a cap is set); masked keys -inf
+                    if (!valid) sv = -INFINITY;
+                    else if (p.softcap > 0.f) sv = p.cap_log2 * tanhf(sv * p.cap_inner);
+                    else sv *= p.scale_log2;
+                    // exponentials against the running reference maximum while the tile maximum
+                    // is reduced; the reference moves (and the row is recomputed) only when the
+                    // tile maximum exceeds it by more than 2^8, so the result is unchanged (the
+                    // final division uses the same reference) and the common tile has no
+                    // maximum -> exponential dependency. l is kept per lane (every lane's share is
+                    // rescaled alike) and summed over the warp once, at the end.
+                    const float m_old = m_run[rr];
+                    float pe = exp2f(sv - (m_old == -INFINITY ? 0.f : m_old));
+                    const float mx = warp_max(sv);
+                    float alpha = 1.f;
+                    if (mx > m_old + kLazyRescaleLog2) {  // the same decision in every lane
+                        alpha = exp2f(m_old - mx);         // 0 while the reference is -inf
+                        m_run[rr] = mx;
+                        pe = exp2f(sv - mx);
+                    }
+                    const __nv_bfloat16 pb = __float2bfloat16_rn(pe);
+                    sP[r * Lay::P_STRIDE + lane] = pb;
+                    l_run[rr] = l_run[rr] * alpha + __bfloat162float(pb);
+                    if (lane == 0) sAlpha[r] = alpha;
+                }
             }
         }
         named_bar_sync(1, kConsumerWarps * 32);
@@ -447,11 +525,21 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
     named_bar_sync(1, kConsumerWarps * 32);
 
     if (clustered) {
-        // Each chunk's unnormalised rows go to its own shared memory (the ring is free: every
-        // tile has been consumed); after a cluster barrier, CTA c merges columns
-        // [c D / n, (c + 1) D / n) of every row over the n chunks:
-        //   M = max_k m_k,  w_k = 2^(m_k - M),  out = sum_k w_k O_k / sum_k w_k l_k
-        float* part = reinterpret_cast<float*>(ring);  // [16][D]
+        // CTA c of the cluster merges the column pairs [c P / n, (c + 1) P / n) (P = D / 2) of
+        // every row over the n chunks:
+        //   M = max_k m_k,  w_k = 2^(m_k - M),  out = sum_k w_k O_k / sum_k w_k l_k.
+        // After one cluster barrier (every chunk has consumed its tiles, so every ring is
+        // free), each chunk sends each owner its rows' part of the owner's slice and its (m, l)
+        // pairs with asynchronous stores that complete on the owner's recv barrier, into the
+        // owner's ring: O_k as [n][16][SW] floats, then (m, l) as [n][16] pairs. The owner
+        // merges from its own shared memory. The second cluster barrier's arrive (release:
+        // this thread's stores have landed) comes before the wait for the slice, and its wait
+        // at the end, so no CTA leaves while a store into it or from it is in flight.
+        const int ns = p.n_split;
+        const int SW = 2 * ((D / 2 + ns - 1) / ns);  // widest slice, in floats
+        float* recvO = reinterpret_cast<float*>(ring);
+        float2* recvML = reinterpret_cast<float2*>(recvO + ns * kRowTile * SW);
+        rows_cluster_sync();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int r = g + 8 * half;
@@ -459,30 +547,37 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
                 const int col = warp * (D / 8) + j * 8 + 2 * tq;
-                *reinterpret_cast<float2*>(part + r * D + col) =
-                    make_float2(o[j][2 * half], o[j][2 * half + 1]);
+                const int owner = merge_owner(col, D, ns);
+                const int c0 = merge_col(owner, D, ns);
+                st_async_v2(rows_map_peer(recvO + (split * kRowTile + r) * SW + (col - c0), owner),
+                            o[j][2 * half], o[j][2 * half + 1], rows_map_peer(recv, owner));
             }
         }
-        rows_cluster_sync();
-        const int ns = p.n_split;
-        const int c0 = split * D / ns, nc = (split + 1) * D / ns - c0;
-        for (int idx = threadIdx.x; idx < n_rows * nc; idx += kConsumerWarps * 32) {
-            const int r = idx / nc, col = c0 + (idx - r * nc);
+        for (int i = threadIdx.x; i < n_rows * ns; i += kConsumerWarps * 32) {
+            const int r = i / ns, dst = i - r * ns;
+            st_async_v2(rows_map_peer(recvML + split * kRowTile + r, dst), sM[r], sL[r],
+                        rows_map_peer(recv, dst));
+        }
+        rows_cluster_arrive_release();
+        const bool got = mbar_wait_cluster(recv, 0, p.err);
+        const int c0 = merge_col(split, D, ns), nc = merge_col(split + 1, D, ns) - c0;
+        for (int idx = threadIdx.x; got && idx < n_rows * nc; idx += kConsumerWarps * 32) {
+            const int r = idx / nc, c = idx - r * nc;
             float M = -INFINITY;
-            for (int k = 0; k < ns; ++k) M = fmaxf(M, ld_cluster_f32(rows_map_peer(sM + r, k)));
+            for (int k = 0; k < ns; ++k) M = fmaxf(M, recvML[k * kRowTile + r].x);
             float L = 0.f, acc = 0.f;
             for (int k = 0; k < ns; ++k) {
-                const float mk = ld_cluster_f32(rows_map_peer(sM + r, k));
-                const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
-                L = fmaf(wk, ld_cluster_f32(rows_map_peer(sL + r, k)), L);
-                acc = fmaf(wk, ld_cluster_f32(rows_map_peer(part + r * D + col, k)), acc);
+                const float2 ml = recvML[k * kRowTile + r];
+                const float wk = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+                L = fmaf(wk, ml.y, L);
+                acc = fmaf(wk, recvO[(k * kRowTile + r) * SW + c], acc);
             }
             const RowInfo ri = row_info(p, len, kvh, row0 + r);
             reinterpret_cast<__nv_bfloat16*>(p.out)[(((size_t)b * p.n_tok + ri.token) * p.n_q +
-                                                     ri.head) * (size_t)D + col] =
+                                                     ri.head) * (size_t)D + c0 + c] =
                 __float2bfloat16_rn(acc / L);
         }
-        rows_cluster_sync();  // peers may still read this CTA's shared memory until here
+        rows_cluster_wait();
         return;
     }
 
