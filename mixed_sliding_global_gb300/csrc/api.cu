@@ -79,8 +79,12 @@ struct Plan {
 
 // Splits of at most this many chunks run as one thread-block cluster per (sequence, KV head)
 // and merge through distributed shared memory; plans of up to twice as many chunks are
-// coarsened to it (one launch and no scratch beat twice the CTAs plus a combine pass).
+// coarsened to it (one launch and no scratch beat twice the CTAs plus a combine pass). When all
+// CTAs of a plan of up to kMaxBigClusterSplit chunks fit on the GPU at once (one per SM), a
+// latency-bound small batch, the plan keeps its chunks and runs as clusters of that many (above
+// the portable cluster size; fewer keys per CTA matter more there than the wider merge).
 constexpr int kMaxClusterSplit = 8;
+constexpr int kMaxBigClusterSplit = 16;
 
 // Decode splits each (sequence, KV head) key range into chunks so that enough CTAs stream
 // the cache at once: about one chunk per SM for small problems, about eight per SM (and at
@@ -110,6 +114,12 @@ Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim,
         n_split = (n_read + chunk - 1) / chunk;
     }
     if (n_split <= 1) return pl;
+    if (n_split <= kMaxBigClusterSplit && (long long)batch * n_kv * n_split <= n_sm) {
+        pl.n_split = (int)n_split;
+        pl.chunk = (int)chunk;
+        pl.cluster = 1;
+        return pl;
+    }
     if (n_split <= 2 * kMaxClusterSplit) {
         if (n_split > kMaxClusterSplit) {
             chunk = round_up((n_read + kMaxClusterSplit - 1) / kMaxClusterSplit, T);

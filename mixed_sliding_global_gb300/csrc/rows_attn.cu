@@ -824,6 +824,10 @@ static cudaError_t launch_bf16_d(const RowsParams& p, dim3 grid, size_t smem, cu
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(rows_attn_bf16_kernel<D, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        // clusters of up to 16 chunks (above the portable 8)
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(rows_attn_bf16_kernel<D, true>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_relaxed);
     }
