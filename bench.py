@@ -48,8 +48,8 @@ PAGE_EXAMPLE = 256      # keys per page of the paged pools
 # of each launch kind (a batch-40 sliding layer in the unsplit launch configuration of the
 # batch-64 one, and a batch-64 global layer); used only while the kernel sources hash to the
 # recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": "d608fb587e0e473cd100d8450436aa145e46bc9a",
-                      "per_algorithmic_byte": {"sliding": 1.0152, "global": 1.0351}}
+NCU_DECODE_TRAFFIC = {"source_sha1": "cca3ae34e7695450fd3b5dfa87b6e9dd4b6652c0",
+                      "per_algorithmic_byte": {"sliding": 1.0163, "global": 1.0346}}
 
 
 # ---------------------------------------------------------------------------------------------

@@ -105,8 +105,6 @@ GEMMA_DEVINL uint32_t map_to_peer(const void* local, uint32_t peer) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(peer));
     return r;
 }
-// Asynchronous 16-byte store into the peer CTA's shared memory; its completion counts 16 bytes
-// of transactions on the peer's mbarrier `mbar` (both cluster shared-memory addresses).
 // two fp32 -> packed fp16 (lo in the low half), round to nearest; values beyond the fp16
 // range saturate to +-65504 instead of becoming infinite
 GEMMA_DEVINL uint32_t pack_f16_sat(float lo, float hi) {
