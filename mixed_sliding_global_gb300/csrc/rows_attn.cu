@@ -581,32 +581,34 @@ __global__ void __launch_bounds__(kRowsThreads, GEMMA_ROWS_MIN_BLOCKS)
         return;
     }
 
+    if constexpr (!CLUSTER) {  // the chunk's rows: final (unsplit) or a partial for the combine
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int r = g + 8 * half;
-        if (r >= n_rows) continue;
-        const RowInfo ri = row_info(p, len, kvh, row0 + r);
-        if (direct) {
-            const float inv = 1.f / sL[r];
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                 (((size_t)b * p.n_tok + ri.token) * p.n_q + ri.head) * (size_t)D;
+        for (int half = 0; half < 2; ++half) {
+            const int r = g + 8 * half;
+            if (r >= n_rows) continue;
+            const RowInfo ri = row_info(p, len, kvh, row0 + r);
+            if (direct) {
+                const float inv = 1.f / sL[r];
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                     (((size_t)b * p.n_tok + ri.token) * p.n_q + ri.head) * (size_t)D;
 #pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                const int col = warp * (D / 8) + j * 8 + 2 * tq;
-                *reinterpret_cast<uint32_t*>(dst + col) =
-                    pack_bf16(o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
-            }
-        } else {
-            const size_t pr = ((size_t)b * p.n_q + ri.head) * p.n_split + split;
-            float* dst = p.o_part + pr * D;
+                for (int j = 0; j < NB; ++j) {
+                    const int col = warp * (D / 8) + j * 8 + 2 * tq;
+                    *reinterpret_cast<uint32_t*>(dst + col) =
+                        pack_bf16(o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
+                }
+            } else {
+                const size_t pr = ((size_t)b * p.n_q + ri.head) * p.n_split + split;
+                float* dst = p.o_part + pr * D;
 #pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                const int col = warp * (D / 8) + j * 8 + 2 * tq;
-                *reinterpret_cast<float2*>(dst + col) = make_float2(o[j][2 * half], o[j][2 * half + 1]);
-            }
-            if (warp == 0 && tq == 0) {
-                p.ml_part[pr * 2 + 0] = sM[r];
-                p.ml_part[pr * 2 + 1] = sL[r];
+                for (int j = 0; j < NB; ++j) {
+                    const int col = warp * (D / 8) + j * 8 + 2 * tq;
+                    *reinterpret_cast<float2*>(dst + col) = make_float2(o[j][2 * half], o[j][2 * half + 1]);
+                }
+                if (warp == 0 && tq == 0) {
+                    p.ml_part[pr * 2 + 0] = sM[r];
+                    p.ml_part[pr * 2 + 1] = sL[r];
+                }
             }
         }
     }
