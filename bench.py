@@ -48,8 +48,8 @@ PAGE_EXAMPLE = 256      # keys per page of the paged pools
 # of each launch kind (a batch-40 sliding layer in the unsplit launch configuration of the
 # batch-64 one, and a batch-64 global layer); used only while the kernel sources hash to the
 # recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": "cca3ae34e7695450fd3b5dfa87b6e9dd4b6652c0",
-                      "per_algorithmic_byte": {"sliding": 1.0163, "global": 1.0346}}
+NCU_DECODE_TRAFFIC = {"source_sha1": "1c8bdee02750be5f2e34501c5f8a00e979df57e3",
+                      "per_algorithmic_byte": {"sliding": 1.0154, "global": 1.0344}}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -305,6 +305,15 @@ class DeviceState:
                                         scale=w.scale(l), workspace=self.ws,
                                         device_error=self.err)
 
+    def layer_step(self, l):
+        """Layer l's launches of a step (append and attention, or the fused launch)."""
+        if self.fused:
+            self.fused_call(l)
+            return
+        if self.w.is_owner(l):
+            self.append_call(l)
+        self.layer_call(l)
+
     def step(self, events=None):
         for l in range(self.w.n_layers):
             if self.fused:
@@ -530,36 +539,75 @@ def logit_run(steps, warmup, device, world, batch=64, rotations=4):
 
 def e2e_run(w, phys, steps, warmup, device, fused=False):
     """Same step through the public API, eager, with this step's inputs copied from pinned host
-    memory and the outputs read back every step (the caches stay resident: they are state)."""
+    memory and the outputs read back every step (the caches stay resident: they are state).
+    The copies run on two copy streams beside the attention launches: layer l's inputs are
+    copied while earlier layers compute, and its output is read back once its launch is done.
+    Events order each buffer's copy against its use, within a step and across steps."""
     st = DeviceState(w, 4321, device, phys, fused=fused)
-    host_in = {}
-    for l in range(w.n_layers):
+    n = w.n_layers
+    host_in = []
+    for l in range(n):
+        pairs = []
         for name in ("q", "k_new", "v_new"):
             t = getattr(st, name)[l]
             if t is not None:
-                host_in[(name, l)] = (t.cpu().pin_memory(), t)
-    lens_h = (st.seq_lens.cpu().pin_memory(), st.seq_lens)
-    wpos_h = (st.write_pos.cpu().pin_memory(), st.write_pos)
+                pairs.append((t.cpu().pin_memory(), t))
+        host_in.append(pairs)
+    meta = [(st.seq_lens.cpu().pin_memory(), st.seq_lens),
+            (st.write_pos.cpu().pin_memory(), st.write_pos)]
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.out]
-    bi = sum(h.numel() * h.element_size() for h, _ in host_in.values()) + 2 * lens_h[0].numel() * 4
+    bi = sum(h.numel() * h.element_size() for pairs in host_in for h, _ in pairs) + \
+        sum(h.numel() * h.element_size() for h, _ in meta)
     bo = sum(h.numel() * h.element_size() for h in host_out)
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    used = [None] * n   # layer l's launches of the previous step are done (its inputs are free)
+    read = [None] * n   # layer l's output of the previous step has been read back
 
-    def one():
-        for h, d in list(host_in.values()) + [lens_h, wpos_h]:
-            d.copy_(h, non_blocking=True)
-        st.step()
-        for h, d in zip(host_out, st.out):
-            h.copy_(d, non_blocking=True)
+    def record(stream):
+        e = torch.cuda.Event()
+        e.record(stream)
+        return e
+
+    def one(after=None):
+        if after is not None:
+            s_in.wait_event(after)   # the timed region's start
+        with torch.cuda.stream(s_in):
+            if used[n - 1] is not None:
+                s_in.wait_event(used[n - 1])   # every layer of the previous step read the lengths
+            for h, d in meta:
+                d.copy_(h, non_blocking=True)
+            in_ev = []
+            for l in range(n):
+                if used[l] is not None:
+                    s_in.wait_event(used[l])
+                for h, d in host_in[l]:
+                    d.copy_(h, non_blocking=True)
+                in_ev.append(record(s_in))
+        for l in range(n):
+            comp.wait_event(in_ev[l])
+            if read[l] is not None:
+                comp.wait_event(read[l])
+            st.layer_step(l)
+            used[l] = record(comp)
+        with torch.cuda.stream(s_out):
+            for l in range(n):
+                s_out.wait_event(used[l])
+                host_out[l].copy_(st.out[l], non_blocking=True)
+                read[l] = record(s_out)
 
     for _ in range(warmup):
         one()
     torch.cuda.synchronize()
     t0, t1 = make_event(False), make_event(False)
     t0.record()
-    for _ in range(steps):
-        one()
+    for k in range(steps):
+        one(t0 if k == 0 else None)
+    comp.wait_stream(s_out)   # the last outputs are back on the host
     t1.record()
     torch.cuda.synchronize()
+    if st.err.item() != 0:
+        raise RuntimeError(f"device error word {st.err.item()} in the end-to-end run")
     ms = t0.elapsed_time(t1) / steps
     del st
     torch.cuda.empty_cache()
