@@ -235,3 +235,48 @@ def test_split_plan_of_the_benchmark_shapes():
     assert g.gemma_attn_workspace_size(64, GLOBAL, 0, 16, 1, 512, 16385, 1) > 0
     assert g.gemma_attn_workspace_size(1, SLIDING, 1024, 16, 8, 256, 8192, 1) == 0
     assert g.gemma_attn_workspace_size(1, GLOBAL, 0, 16, 1, 512, 8192, 1) > 0
+
+
+# ------------------------------------------------------------------------------------------
+# small grids whose split merges inside one thread-block cluster of 9 to 16 chunks (above the
+# portable cluster size): every head_dim, K and V or K as V, both kinds, fused append included
+# ------------------------------------------------------------------------------------------
+BIG_CLUSTER_SHAPES = [
+    # (spec, lens after the append, capacity); chunks = ceil(max len / 32) <= 16 and
+    # batch x n_kv x chunks <= 152, so the plan keeps every chunk and merges in the cluster
+    (LayerSpec(GLOBAL, 0, 8, 2, 64, False), [300, 450], 512),
+    (LayerSpec(GLOBAL, 0, 16, 4, 128, True), [500], 512),
+    (LayerSpec(SLIDING, 512, 16, 8, 256, False), [2000], 2048),
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), [350, 500, 129], 512),
+    (LayerSpec(SLIDING, 300, 8, 1, 512, False), [1000, 290], 1024),
+]
+
+
+@pytest.mark.parametrize("case", range(len(BIG_CLUSTER_SHAPES)))
+def test_decode_in_big_clusters(case):
+    import mixed_sliding_global_gb300 as g
+    spec, lens, cap = BIG_CLUSTER_SHAPES[case]
+    w = one_layer(spec, 1, lens, cap)
+    msl = max(lens)
+    n_read = min(spec.window, msl) if spec.kind == SLIDING else msl
+    chunks = -(-n_read // 32)
+    assert 8 < chunks <= 16 and len(lens) * spec.n_kv * chunks <= 152
+    # a cluster plan needs no scratch
+    assert g.gemma_attn_workspace_size(len(lens), spec.kind, spec.window, spec.n_q, spec.n_kv,
+                                       spec.head_dim, msl, 1) == 0
+    run_and_compare(w, [0])
+    # the same launch with the step's K/V row written inside it
+    hb = host_inputs(w, [0])
+    ref = oracle_outputs(w, hb, [0])
+    gr = DeviceRun(w, hb)
+    d = gr.dev[0]
+    out = torch.empty_like(d["q"])
+    g.gemma_attn_decode_append(out, d["q"], gr.kc, gr.vc, w.owner_map, 0, d["k_new"],
+                               d.get("v_new"), d["write_pos"], d["seq_lens"], msl,
+                               kind=spec.kind, window=spec.window, n_kv=spec.n_kv,
+                               k_eq_v=spec.k_eq_v, scale=w.scale(0),
+                               workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"),
+                               device_error=gr.err)
+    torch.cuda.synchronize()
+    assert gr.err.item() == 0
+    compare(out.cpu(), ref[0], BF16)
