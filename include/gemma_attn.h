@@ -119,7 +119,11 @@ int gemma_kv_append_ring(void* const* k_cache, void* const* v_cache, const int32
  *                     owner_map[owner_map[l]] == owner_map[l]. The owner must have this
  *                     layer's kind, n_kv, head_dim and k_eq_v (the caller's contract).
  *   seq_lens          DEVICE int32[batch], 1 <= seq_lens[b] <= max_seq_len.
- *   max_seq_len       HOST bound on seq_lens, used to plan the split over keys.
+ *   max_seq_len       HOST bound on seq_lens, used to plan the split over keys: unsplit when
+ *                     the (sequence, KV head) pairs alone fill the GPU over short key ranges;
+ *                     else chunks of keys merged inside the launch when a pair's chunks form
+ *                     one thread-block cluster (at most 8, or 16 when the whole grid fits one
+ *                     CTA per SM), else by a second launch through the workspace.
  *   scale             softmax scale applied to q . k, finite and > 0 (1/sqrt(head_dim) in
  *                     the workloads).
  *   workspace         DEVICE scratch of at least
@@ -148,7 +152,8 @@ int gemma_attn_decode(void* out, const void* q, const void* const* k_cache,
  *  - Returns GEMMA_ERR_WORKSPACE, with no launch, when the arguments are valid but
  *    gemma_attn_workspace_size(...) for them is larger than 32 MiB (e.g. batch 64 x 16 query
  *    heads of head_dim 512 split 19 ways needs about 40 MB and is refused; batch-1 plans need
- *    a few MB at most, and plans of up to 8 chunks need none).
+ *    a few MB at most, and plans whose chunks merge inside one thread-block cluster need
+ *    none).
  *  - The first call in each CUDA context (per device, and again after a device reset) looks up
  *    the array's device address with that device current; make that first call before any
  *    stream capture.
