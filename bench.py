@@ -112,12 +112,15 @@ def kernel_source_sha1():
 # clocks during the timed region
 # ---------------------------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 20 ms; only those stamped inside [start(), stop()] count (the
+    sampler is running, its first line read, before start() returns)."""
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device):
         self.proc = None
+        self.first = ""
         try:
             self.uuid = str(torch.cuda.get_device_properties(device).uuid)
         except Exception:
@@ -127,31 +130,45 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.first = self.proc.stdout.readline()   # sampling has begun
         except (OSError, ValueError):
             self.proc = None
+        self.t0 = time.time()
+
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
+        t1 = time.time()
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
-        mine = [r for r in rows if self.uuid and self.uuid.replace("GPU-", "") in r[0]] or rows
-        if not mine:
+        rows = [r.split(",") for r in (self.first + out).strip().splitlines() if r.count(",") >= 9]
+        mine = [r for r in rows if self.uuid and self.uuid.replace("GPU-", "") in r[1]] or rows
+        inside = [r for r in mine if (lambda t: t is not None and self.t0 <= t <= t1)(self._stamp(r[0]))]
+        use = inside or mine
+        if not use:
             return None
-        sm = [float(r[1]) for r in mine if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in mine if r[2].strip().replace(".", "").isdigit()]
+        sm = [float(r[2]) for r in use if r[2].strip().replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in use if r[3].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in mine for n, v in zip(names, r[5:9]) if "Active" in v
+        reasons = sorted({n for r in use for n, v in zip(names, r[6:10]) if "Active" in v
                           and "Not" not in v})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(mine)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "samples_around": len(mine)}
 
 
 # ---------------------------------------------------------------------------------------------
