@@ -281,7 +281,7 @@ size_t gemma_attn_workspace_size(int batch, gemma_layer_kind kind, int window, i
  *               block_table[b * max_pages + p / page_size], row p % page_size. The same table
  *               may serve every layer. Entries are read only for the pages that hold keys a
  *               step attends or writes (from the window start rounded down to a multiple of 32
- *               keys, 128 for prefill, to the last position), so pages wholly before a sliding
+ *               keys, 64 for prefill, to the last position), so pages wholly before a sliding
  *               window may be recycled by the caller. An entry outside [0, n_pages) that is read
  *               sets GEMMA_DEVERR_PAGE; its rows read as zeros and are never written.
  *   page_size   a multiple of 128 (GEMMA_ERR_UNSUPPORTED otherwise): no key tile crosses a page.
