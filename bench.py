@@ -453,9 +453,11 @@ def workload(name, batch=None, layers=None, offset=0, max_len=None):
 
 
 def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rotations=1,
-                    softcap=None, n_real=None, fused=False, ring=None, paged=None):
-    """Capture one graph per step (rotating over `rotations` independent input copies) and
-    time `steps` replays after `warmup` replays. Returns step time and, with per_launch, the
+                    softcap=None, n_real=None, fused=False, ring=None, paged=None, min_ms=None):
+    """Capture one graph per input copy (rotating over `rotations` independent copies) and
+    time `steps` replays after `warmup` replays; with min_ms, as many more steps as make the
+    timed region last about min_ms (so that the clock samples fall inside it; the returned
+    info holds the count). Returns step time and, with per_launch, the
     mean duration of each layer's attention launch, taken in a second pass of `steps` replays
     of graphs with an event pair around every launch (event nodes cost a few microseconds
     each and break the overlap of consecutive launches, so the step time is taken without
@@ -468,18 +470,27 @@ def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rot
     for st in states:
         if st.err.item() != 0:
             raise RuntimeError(f"device error word {st.err.item()} in the eager pass")
-    graphs = [capture(states[k % rotations]) for k in range(warmup + steps)]
+    graphs = [capture(st) for st in states]
+    steps_asked = steps
     torch.cuda.synchronize()
     for k in range(warmup):
-        graphs[k].replay()
+        graphs[k % rotations].replay()
+    if min_ms is not None:
+        c0, c1 = make_event(False), make_event(False)
+        c0.record()
+        for k in range(rotations):
+            graphs[k].replay()
+        c1.record()
+        torch.cuda.synchronize()
+        steps = max(steps, int(min_ms / max(c0.elapsed_time(c1) / rotations, 1e-3)) + 1)
     clocks = ClockSampler(torch.cuda.current_device())
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     t0, t1 = make_event(False), make_event(False)
     t0.record()
-    for k in range(warmup, warmup + steps):
-        graphs[k].replay()
+    for k in range(steps):
+        graphs[k % rotations].replay()
     t1.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -488,29 +499,30 @@ def timed_graph_run(w, phys, steps, warmup, device, world, per_launch=False, rot
     del graphs
     launch_ms = None
     if per_launch:
+        n_ev = steps_asked
         ev = [[(make_event(True), make_event(True)) for _ in range(w.n_layers)]
-              for _ in range(steps)]
-        eg = [capture(states[k % rotations], ev[k]) for k in range(steps)]
-        for k in range(min(warmup, steps)):
+              for _ in range(n_ev)]
+        eg = [capture(states[k % rotations], ev[k]) for k in range(n_ev)]
+        for k in range(min(warmup, n_ev)):
             eg[k].replay()
         torch.cuda.synchronize()
-        for k in range(steps):
+        for k in range(n_ev):
             eg[k].replay()
         torch.cuda.synchronize()
-        launch_ms = [sum(ev[k][l][0].elapsed_time(ev[k][l][1]) for k in range(steps)) / steps
+        launch_ms = [sum(ev[k][l][0].elapsed_time(ev[k][l][1]) for k in range(n_ev)) / n_ev
                      for l in range(w.n_layers)]
         del eg
     for st in states:
         if st.err.item() != 0:
             raise RuntimeError(f"device error word {st.err.item()} after the timed region")
     info = {"launches_per_step": states[0].launches_per_step(),
-            "cache_bytes": sum(s.cache_bytes for s in states)}
+            "cache_bytes": sum(s.cache_bytes for s in states), "steps": steps}
     del states
     torch.cuda.empty_cache()
     return ms, launch_ms, clk, info
 
 
-def logit_run(steps, warmup, device, world, batch=64, rotations=4):
+def logit_run(steps, warmup, device, world, batch=64, rotations=4, min_ms=None):
     """The greedy step after the LM head: final-logit soft-cap (cap 30, written out) and argmax
     of [64][262144] bf16 logits, rotating over `rotations` input/output pairs (together larger
     than L2), each call captured in one graph. Returns time per call and launches per call."""
@@ -534,6 +546,14 @@ def logit_run(steps, warmup, device, world, batch=64, rotations=4):
             call(r)
     for _ in range(warmup):
         g.replay()
+    if min_ms is not None:
+        # as many replays as make the timed region last about min_ms (clock samples inside)
+        c0, c1 = make_event(False), make_event(False)
+        c0.record()
+        g.replay()
+        c1.record()
+        torch.cuda.synchronize()
+        steps = max(steps, int(min_ms / max(c0.elapsed_time(c1), 1e-3)) + 1)
     clocks = ClockSampler(torch.cuda.current_device())
     barrier(world)
     torch.cuda.synchronize()
@@ -551,7 +571,7 @@ def logit_run(steps, warmup, device, world, batch=64, rotations=4):
     bytes_per_call = batch * V * 2 * 2 + batch * 4
     del g, xs, outs
     torch.cuda.empty_cache()
-    return ms, bytes_per_call, 2 if n_split > 1 else 1, clk
+    return ms, bytes_per_call, 2 if n_split > 1 else 1, clk, steps
 
 
 def e2e_run(w, phys, steps, warmup, device, fused=False):
@@ -728,7 +748,7 @@ def run_logits(args):
     build_library(world, local)
     device = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    ms, nbytes, launches, clk = logit_run(args.steps, args.warmup, device, world)
+    ms, nbytes, launches, clk, lsteps = logit_run(args.steps, args.warmup, device, world)
     ms = max_over_ranks(ms, world)
     v = world * nbytes / (ms * 1e-3) / 1e9
     line = {"metric": "logit soft-cap + argmax HBM GB/s", "value": v, "unit": "GB/s",
@@ -958,7 +978,8 @@ def run_native(args):
             ms2, lm2, clk2, info2 = timed_graph_run(w2, phys2, args.steps, args.warmup, device,
                                                     world, per_launch=(w2.n_new > 1),
                                                     rotations=rot, softcap=cap2, n_real=real2,
-                                                    fused=fused2, ring=ring2, paged=paged2)
+                                                    fused=fused2, ring=ring2, paged=paged2,
+                                                    min_ms=60.0)
             ms2 = max_over_ranks(ms2, world)
             d2 = w2.n_new == 1
             u2, sc2 = ("GB/s", 1e9) if d2 else ("TFLOP/s", 1e12)
@@ -967,7 +988,7 @@ def run_native(args):
                    "frac": v2 / (peaks["hbm_gbs"] if d2 else peaks["bf16_tflops_sustained"]),
                    "us_per_layer_step": 1e3 * ms2 / w2.n_layers,
                    "gpu_launches_per_step": info2["launches_per_step"],
-                   "clocks": clk2}
+                   "steps": info2["steps"], "clocks": clk2}
             if lm2 is not None:
                 ach = sum(prefill_flops(w2, l, real2) for l in range(w2.n_layers)) / \
                     (sum(lm2) * 1e-3) / 1e12
@@ -996,14 +1017,15 @@ def run_native(args):
             also[name] = ent
         # the greedy step after the LM head: final-logit soft-cap 30 (capped logits written)
         # and argmax over the pages' 262,144-token vocabulary, batch 64, bf16
-        lms, lbytes, llaunch, lclk = logit_run(args.steps, args.warmup, device, world)
+        lms, lbytes, llaunch, lclk, lsteps = logit_run(args.steps, args.warmup, device, world,
+                                                       min_ms=60.0)
         lms = max_over_ranks(lms, world)
         lv = world * lbytes / (lms * 1e-3) / 1e9
         also["logit_softcap_argmax"] = {
             "value": lv, "unit": "GB/s", "ms_per_step": lms, "frac": lv / peaks["hbm_gbs"],
             "config": {"batch": 64, "vocab": synth.VOCAB, "softcap": synth.LOGIT_SOFTCAP,
                        "dtype": "bf16", "capped_output": True},
-            "bytes_per_call": lbytes, "gpu_launches_per_step": llaunch,
+            "bytes_per_call": lbytes, "gpu_launches_per_step": llaunch, "steps": lsteps,
             "l2": "4 rotating input/output pairs (268 MB)", "clocks": lclk}
         line["also"] = also
     if rank == 0:
