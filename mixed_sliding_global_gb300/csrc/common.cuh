@@ -181,6 +181,36 @@ GEMMA_DEVINL float warp_sum(float v) {
     return v;
 }
 
+// Three-input maximum (NaN inputs ignored as by fmaxf).
+GEMMA_DEVINL float fmax3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// Two fp32 lanes in one 64-bit register, and packed fused multiply-add / add on them (each
+// lane rounded to nearest, as two scalar operations would be).
+GEMMA_DEVINL unsigned long long f32x2(float lo, float hi) {
+    unsigned long long v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+    return v;
+}
+GEMMA_DEVINL float2 f32x2_split(unsigned long long v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+GEMMA_DEVINL unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                          unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+GEMMA_DEVINL unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // 2^x with the SFU's approximate exp2 (flushes denormal results to zero; -inf gives 0).
 GEMMA_DEVINL float fast_exp2(float x) {
     float y;

@@ -682,15 +682,22 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                             if (key < lo || key >= hi) s[e] = -INFINITY;
                         }
                     }
+                    // (three-input maxima and, below, packed two-lane fp32 arithmetic: fewer
+                    // instructions from these warps, which share issue slots with the MMA
+                    // issuer)
+                    static_assert(kFaKeys == 64, "the reduction below covers 64 keys");
                     float mx8[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3f(s[i], s[8 + i], s[16 + i]);
 #pragma unroll
-                    for (int e = 8; e < kFaKeys; e += 8)
+                    for (int e = 24; e < 56; e += 16)
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[e + i]);
-                    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                        for (int i = 0; i < 8; ++i) mx8[i] = fmax3f(mx8[i], s[e + i], s[e + 8 + i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[56 + i]);
+                    const float mx = fmax3f(fmax3f(mx8[0], mx8[1], mx8[2]),
+                                            fmax3f(mx8[3], mx8[4], mx8[5]),
+                                            fmaxf(mx8[6], mx8[7])) *
                                      sl2;
 
                     // ---- the row's reference after tile T-1, then after tile T ----
@@ -725,15 +732,18 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                     }
                     // ---- P(T) = 2^(s * scale_log2 - m) into shared memory buffer T % 2 ----
                     const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
-                    float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                    const unsigned long long sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
+                    unsigned long long sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
                     uint32_t pw[kFaKeys / 2];
 #pragma unroll
                     for (int k2 = 0; k2 < kFaKeys / 2; ++k2) {
-                        const float p0 = fast_exp2(fmaf(s[2 * k2], sl2, neg_m));
-                        const float p1 = fast_exp2(fmaf(s[2 * k2 + 1], sl2, neg_m));
-                        sum4[k2 & 3] += p0 + p1;
+                        const float2 x = f32x2_split(fma_f32x2(f32x2(s[2 * k2], s[2 * k2 + 1]), sl2x2, negm2));
+                        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                        sum2[k2 & 1] = add_f32x2(sum2[k2 & 1], f32x2(p0, p1));
                         pw[k2] = pack_bf16(p0, p1);
                     }
+                    const float2 sa = f32x2_split(sum2[0]), sb = f32x2_split(sum2[1]);
+                    const float sum4[4] = {sa.x, sa.y, sb.x, sb.y};
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<uint4*>(sPw + r * 128 + ((c ^ (r & 7)) * 16)) =
