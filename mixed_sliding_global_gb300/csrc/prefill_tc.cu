@@ -651,8 +651,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float2 f = unpack_f16(wd[i]);
-                                s[8 * c + 2 * i] += f.x;
-                                s[8 * c + 2 * i + 1] += f.y;
+                                const float2 t = f32x2_split(add_f32x2(
+                                    f32x2(s[8 * c + 2 * i], s[8 * c + 2 * i + 1]), f32x2(f.x, f.y)));
+                                s[8 * c + 2 * i] = t.x;
+                                s[8 * c + 2 * i + 1] = t.y;
                             }
                         }
                         // every lane has consumed its loads of X[w] (the adds above): the peer may
@@ -669,9 +671,19 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                     if (SOFTCAP) {
                         const float k2 = 2.8853900817779268f * p.cap_inner;  // 2 log2(e) s / c
                         const float c2 = 2.f * p.cap_log2;
+                        const unsigned long long k2x2 = f32x2(k2, k2), zero2 = f32x2(0.f, 0.f),
+                                                 one2 = f32x2(1.f, 1.f), mc2 = f32x2(-c2, -c2),
+                                                 cl2 = f32x2(p.cap_log2, p.cap_log2);
 #pragma unroll
-                        for (int e = 0; e < kFaKeys; ++e)
-                            s[e] = fmaf(-c2, fast_rcp(fast_exp2(s[e] * k2) + 1.f), p.cap_log2);
+                        for (int e = 0; e < kFaKeys; e += 2) {
+                            const float2 a = f32x2_split(fma_f32x2(f32x2(s[e], s[e + 1]), k2x2, zero2));
+                            const float2 b = f32x2_split(
+                                add_f32x2(f32x2(fast_exp2(a.x), fast_exp2(a.y)), one2));
+                            const float2 o = f32x2_split(
+                                fma_f32x2(mc2, f32x2(fast_rcp(b.x), fast_rcp(b.y)), cl2));
+                            s[e] = o.x;
+                            s[e + 1] = o.y;
+                        }
                         sl2 = 1.f;
                     }
                     const int kt0 = cur.k_begin + t * kFaKeys;
