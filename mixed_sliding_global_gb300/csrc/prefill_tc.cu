@@ -735,9 +735,14 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                             uint32_t v[32];
                             tmem_ld32(tO + lane_off + j * 32, v);
                             tmem_ld_wait();
+                            const unsigned long long alpha2 = f32x2(alpha, alpha);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            for (int e = 0; e < 32; e += 2) {
+                                const float2 o = f32x2_split(mul_f32x2(
+                                    f32x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), alpha2));
+                                v[e] = __float_as_uint(o.x);
+                                v[e + 1] = __float_as_uint(o.y);
+                            }
                             tmem_st32(tO + lane_off + j * 32, v);
                         }
                         tmem_st_wait();
@@ -805,13 +810,19 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                             tmem_ld32(tO + lane_off + w * (DH / 2) + sl * SW + j * 32, v);
                             tmem_ld_wait();
 #pragma unroll
+                            const unsigned long long inv2 = f32x2(inv, inv);
                             for (int e = 0; e < 4; ++e) {
                                 const int c = j * 4 + e;
-                                *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) * 16)) = make_uint4(
-                                    pack_bf16(__uint_as_float(v[8 * e + 0]) * inv, __uint_as_float(v[8 * e + 1]) * inv),
-                                    pack_bf16(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv),
-                                    pack_bf16(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv),
-                                    pack_bf16(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv));
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const float2 o = f32x2_split(mul_f32x2(
+                                        f32x2(__uint_as_float(v[8 * e + 2 * q]), __uint_as_float(v[8 * e + 2 * q + 1])),
+                                        inv2));
+                                    w4[q] = pack_bf16(o.x, o.y);
+                                }
+                                *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) * 16)) =
+                                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
                         }
                         __syncwarp();
