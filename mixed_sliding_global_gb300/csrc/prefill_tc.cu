@@ -26,7 +26,7 @@
 // K/V tiles have landed and P(i-2) is written; the MMA warp commits step_done[i] after the
 // step's MMAs. A tcgen05.mma is accepted only when the one before it is nearly done, so each
 // wait or commit between MMA groups idles the tensor core: the MMA warp does one of each per
-// step. Within a step, each 64-column block of S is followed by one of the (longer) P V MMAs:
+// step. Within a step, each 64-column block of S is preceded by one of the (longer) P V MMAs:
 // the issuing thread shares its SM sub-partition with softmax warps, and a long MMA gives it
 // time to be scheduled before the pipe runs dry.
 // TMEM (512 columns): Q (DH/2 columns of packed bf16) at 0, S buffers at 128 and 192 (64 fp32
@@ -460,21 +460,21 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                     if (lane == 0) issue_s(cur, i);
                 } else if (lane == 0) {
                     if (cur.valid && h2.valid) {
-                        // S(i) and P V(i-2) interleaved: a long P V MMA after every 64 columns of S
+                        // S(i) and P V(i-2) interleaved: a long P V MMA before every 64 columns of S
                         const uint64_t kd = smem_desc_sw128(smem_u32(slots + cur.slot * Lay::SLOT), 0, 1024);
                         const uint32_t tS = tmem + Lay::S_COL + 64 * (i & 1);
                         const uint64_t vd = smem_desc_sw128(smem_u32(slots + h2.slot * Lay::SLOT), Lay::BOX, 1024);
                         const uint64_t pd = smem_desc_sw128(smem_u32(sP + (i & 1) * Lay::P_TILE), 0, 1024);
 #pragma unroll
                         for (int c = 0; c < Lay::CHUNKS; ++c) {
+                            if (c < kFaKeys / 16)
+                                umma_ss(tO, pd + (uint64_t)((c * 32) >> 4), vd + (uint64_t)((c * 2048) >> 4),
+                                        id_pv, (!h2.first || c > 0) ? 1u : 0u);
 #pragma unroll
                             for (int ks = 0; ks < 4; ++ks)
                                 umma_ts(tS, tQ + c * 32 + ks * 8,
                                         kd + (uint64_t)((c * Lay::BOX + ks * 32) >> 4), id_qk,
                                         (c | ks) ? 1u : 0u);
-                            if (c < kFaKeys / 16)
-                                umma_ss(tO, pd + (uint64_t)((c * 32) >> 4), vd + (uint64_t)((c * 2048) >> 4),
-                                        id_pv, (!h2.first || c > 0) ? 1u : 0u);
                         }
 #pragma unroll
                         for (int kk = Lay::CHUNKS; kk < kFaKeys / 16; ++kk)
