@@ -1,0 +1,792 @@
+// prefill_pair.cu -- prefill-bucket attention at head_dim 256 on CTA pairs (the 2-SM form of the
+// 5th-generation tensor-core MMA, tcgen05 with cta_group::2).
+//
+// Computes, for tiles of 256 query rows (rows = (token, head of the GQA group) pairs, token
+// major, so every row of a tile reads the same KV head), softmax(scale * Q K^T) V over the
+// causal (and, on sliding layers, windowed) key range of each row, with the K/V cache of the
+// owner layer ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", sections 2.1-2.3; the
+// pages' "eager" matmul-softmax-matmul definition, section 4.3). The sliding layers of every
+// Gemma-4 size have head_dim 256.
+//
+// A cluster of two CTAs (one per SM) runs each MMA as one instruction of M = 256: CTA c owns
+// rows 128c..128c+127 of the tile (its Q rows in its tensor memory, its rows of S and O in its
+// tensor memory, its rows of P in its shared memory), and each CTA holds half of every B
+// operand. Per 128-key tile:
+//   S = Q K^T   N = 128 keys: CTA c holds keys 64c..64c+63 of K (all 256 columns, 32 KB);
+//   O += P V    N = 256 columns: CTA c holds columns 128c..128c+127 of V (all 128 keys, 32 KB).
+// So a 128-key step needs 64 KB of shared memory per SM (a one-SM 128-key step needs 128 KB),
+// S runs at N = 128 (an MMA of N = 64 costs as much as one of N = 128), and one step issues 24
+// MMAs where one-SM 64-key steps issue 40 for the same keys.
+//
+// Persistent grid: each pair walks work units = (256-row tile, sequence, KV head), latest row
+// tiles (longest key ranges) first; the 128-key tiles of all its units form one flat sequence.
+// Warps of each CTA:
+//   warps 0-7   softmax: thread r of warpgroup w owns row r (TMEM lane r) and the 64 columns
+//               64w..64w+63 of each S tile, and columns 128w..128w+127 of O. The two groups
+//               swap their row maxima through shared memory; the row's softmax reference moves
+//               only when a tile maximum exceeds it by more than 2^8 (lazy rescaling keeps the
+//               result exact: the final division uses the same reference), and O rows are
+//               rescaled in TMEM when it moves. P goes to shared memory as bf16.
+//   warp 8      TMA producer: this CTA's halves of the K and V tiles (128-byte swizzle, boxes of
+//               64 keys x 64 columns) into a FIFO ring of 32 KB slots, in the MMA order.
+//   warp 9      even CTA: issues S(t) = Q K(t)^T once both CTAs' softmax warps have read S(t-1),
+//               so the softmax of tile t overlaps the P V of tile t-1 and the S of tile t+1.
+//               Odd CTA: forwards each of its ring slots' arrivals to the even CTA's barriers
+//               (an MMA reads both CTAs' halves).
+//   warp 10     even CTA: issues O += P(t) V(t) once both CTAs' P(t) is in shared memory.
+// Barriers that the issuers wait on live in the even CTA and count arrivals from both CTAs;
+// the issuers' commits arrive on the same barrier in both CTAs (multicast). Arrivals from the
+// odd CTA are plain remote arrivals: a thread that wrote shared memory an MMA reads (P, zeroed
+// V rows) orders those writes before the async proxy with a proxy fence first, and one that
+// read or wrote tensor memory fences its tcgen05 operations before the arrival.
+// TMEM (512 columns per CTA): Q (128 columns of packed bf16) at 0, S (128 fp32) at 128, O (256
+// fp32) at 256.
+//
+// The key range of a unit is clamped to [first row's window start, last row's position] before
+// any load; rows of a V tile outside the range are zeroed in shared memory before they enter
+// P V (they may hold anything, NaN included).
+#include <atomic>
+
+#include "attn_internal.h"
+#include "tc.cuh"
+#include "tmap.h"
+
+namespace gemma {
+
+namespace {
+
+constexpr int kPrD = 256;
+constexpr int kPrWarps = 11;
+constexpr int kPrThreads = kPrWarps * 32;
+constexpr int kPrProducerWarp = 8;
+constexpr int kPrSWarp = 9;     // S issuer (even CTA) / slot forwarder (odd CTA)
+constexpr int kPrPvWarp = 10;   // P V issuer (even CTA)
+constexpr int kPrKeys = 128;                  // keys per tile (N of S)
+constexpr int kPrRows = 256;                  // rows per unit (M of the pair's MMAs)
+constexpr int kPrBox = 64 * 128;              // TMA box: 64 keys x 64 columns of bf16
+constexpr int kPrSlot = 4 * kPrBox;           // K half (64 keys x 256) or V half (128 x 128)
+constexpr int kPrPTile = 128 * kPrKeys * 2;   // P: 128 rows x 128 keys bf16
+constexpr int kPrSlots = 5;
+constexpr int kPrSmemLimit = 232448;          // max dynamic shared memory per block
+constexpr float kPrLazyLog2 = 8.f;
+constexpr int kPrQCol = 0, kPrSCol = 128, kPrOCol = 256;  // TMEM columns
+// shared memory: ring, P, row maxima [2 tiles][2 groups][128], row sums [2][128], barriers
+constexpr int kPrBarOff = kPrSlots * kPrSlot + kPrPTile + (2 * 2 * 128 + 2 * 128) * 4;
+constexpr int kPrSmem = kPrBarOff + 256 + 1024;  // + barriers, + alignment slack
+static_assert(kPrSmem <= kPrSmemLimit, "shared memory budget");
+
+struct PrParams {
+    RowsParams p;
+    int batch;
+    int n_rt;      // 256-row tiles per (sequence, KV head)
+    int n_units;   // n_rt * batch * n_kv
+    int n_pairs;   // clusters walking the units
+};
+
+struct PrUnit {
+    int b, kvh, rt, row0;
+    int n_rows;       // rows of the bucket this unit writes
+    int n_rows_real;  // rows that attend (the rest are pad rows or a bad sequence: zeros)
+    int len, n_real;
+    bool bad, bad_real;
+    int k_begin, k_end, n_tiles;
+    int n_head;       // leading keys of the first tile before every row's window (aligned start)
+};
+
+// Unit u: row tiles from the last (longest key ranges) to the first, then sequences, then KV
+// heads.
+__device__ __forceinline__ PrUnit pr_unit(const PrParams& fp, int u) {
+    const RowsParams& p = fp.p;
+    PrUnit U;
+    const int per_rt = fp.batch * p.n_kv;
+    const int q = u / per_rt, rem = u - q * per_rt;
+    U.rt = fp.n_rt - 1 - q;
+    U.b = rem / p.n_kv;
+    U.kvh = rem - U.b * p.n_kv;
+    const int rows_total = p.n_tok * p.G;
+    U.row0 = U.rt * kPrRows;
+    U.n_rows = min(kPrRows, rows_total - U.row0);
+    U.len = __ldg(p.seq_lens + U.b);
+    // real tokens of this sequence (a padded bucket's first n_real rows; all rows otherwise);
+    // the i-th real token sits at len - n_real + i, the pad rows' outputs are zero
+    U.n_real = p.n_real ? __ldg(p.n_real + U.b) : p.n_tok;
+    U.bad_real = U.n_real < 0 || U.n_real > p.n_tok;
+    U.bad = U.bad_real || U.len < U.n_real || (!p.ring && U.len > p.cap) || U.len > p.max_seq_len;
+    U.n_rows_real = U.bad ? 0 : max(0, min(kPrRows, U.n_real * p.G - U.row0));
+    // key range: from the first row's window start to the last real row's position (a ring
+    // cache's or paged pool's 64-key groups start at multiples of 64, so that none wraps around
+    // the ring or crosses a page; the rows' masks drop the keys before the window)
+    const int tok_first = U.row0 / p.G;
+    const int tok_last = (U.row0 + max(U.n_rows_real, 1) - 1) / p.G;
+    const int pos_first = U.len - U.n_real + tok_first;
+    const int lo_first = p.is_sliding ? max(0, pos_first - p.window + 1) : 0;
+    U.k_begin = (p.ring || p.page_size) ? (lo_first & ~63) : lo_first;
+    U.k_end = U.len - U.n_real + tok_last + 1;
+    U.n_tiles = U.n_rows_real == 0 ? 0 : (U.k_end - U.k_begin + kPrKeys - 1) / kPrKeys;
+    U.n_head = lo_first - U.k_begin;
+    return U;
+}
+
+// One tile of the flat per-pair sequence, as the producer and the issuers see it.
+struct PrTile {
+    bool valid, first, last;
+    int ord;       // ordinal of its unit among this pair's units that have tiles
+    int n_valid;   // keys of the tile inside the unit's range (the rest are zeroed in V)
+    int n_head;    // leading keys zeroed (first tile of an aligned-start unit)
+    int key0;      // first key
+    int b, kvh;
+};
+
+struct PrTileIter {
+    int u, stride, t, ord;
+    PrUnit U;
+    __device__ __forceinline__ void init(const PrParams& fp, int worker) {
+        u = worker - fp.n_pairs;  // next() advances to the first unit
+        stride = fp.n_pairs;
+        t = 0;
+        ord = -1;
+        U.n_tiles = 0;
+    }
+    __device__ __forceinline__ PrTile next(const PrParams& fp) {
+        PrTile T;
+        T.valid = false;
+        while (t >= U.n_tiles) {
+            u += stride;
+            if (u >= fp.n_units) return T;
+            U = pr_unit(fp, u);
+            t = 0;
+            if (U.n_tiles > 0) ++ord;
+        }
+        T.valid = true;
+        T.first = t == 0;
+        T.last = t == U.n_tiles - 1;
+        T.ord = ord;
+        T.key0 = U.k_begin + t * kPrKeys;
+        T.n_valid = min(kPrKeys, U.k_end - T.key0);
+        T.n_head = t == 0 ? U.n_head : 0;
+        T.b = U.b;
+        T.kvh = U.kvh;
+        ++t;
+        return T;
+    }
+};
+
+}  // namespace
+
+// SOFTCAP: the soft-capped variant (a separate instantiation, so that the plain kernel carries
+// no code for it)
+template <bool SOFTCAP>
+__global__ void __launch_bounds__(kPrThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const PrParams fp) {
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel on the stream (the append of these rows) has completed
+    const RowsParams& p = fp.p;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* slots = smem;
+    uint8_t* sP = smem + kPrSlots * kPrSlot;                          // [2 key blocks][128][64]
+    float* mxs = reinterpret_cast<float*>(sP + kPrPTile);             // [2][2][128]
+    float* lxs = mxs + 2 * 2 * 128;                                   // [2][128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPrBarOff);
+    // ring slot s: full[s] completes when this CTA's half has landed (producer arrival +
+    // transaction bytes); pfull[s] (even CTA) when the odd CTA's half has (its warp 9 forwards
+    // its own full[s]); empty[s] when the MMAs that read the slot have completed (multicast).
+    uint64_t* full = bars;
+    uint64_t* pfull = bars + kPrSlots;
+    uint64_t* empty = bars + 2 * kPrSlots;
+    uint64_t* s_full = bars + 3 * kPrSlots;  // S(t) is in TMEM (multicast commit)
+    uint64_t* s_free = s_full + 1;           // even CTA: both CTAs' softmax warps have read S(t)
+    uint64_t* p_full = s_full + 2;           // even CTA: both CTAs' P(t) is in shared memory
+    uint64_t* pv_done = s_full + 3;          // P V(t) has completed (multicast commit)
+    uint64_t* o_full = s_full + 4;           // a unit's last P V has completed (multicast)
+    uint64_t* o_free = s_full + 5;           // even CTA: both epilogues have read O
+    uint64_t* q_ready = s_full + 6;          // even CTA: both CTAs' Q rows are in TMEM
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(s_full + 7);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t c = cluster_rank();       // 0: issues the pair's MMAs
+    const int worker = blockIdx.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPrSlots; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&pfull[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 16);  // 8 softmax warps per CTA
+        mbar_init(p_full, 16);
+        mbar_init(pv_done, 1);
+        mbar_init(o_full, 1);
+        mbar_init(o_free, 16);
+        mbar_init(q_ready, 16);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // both CTAs run and their barriers exist before the pair allocation, any remote arrival or
+    // any multicast commit
+    cluster_sync();
+    if (warp == kPrSWarp) {  // one warp in each CTA, together
+        tmem_alloc_pair(tslot, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    // rows of a V tile outside the unit's key range, zeroed (whole warp)
+    auto zero_v = [&](uint8_t* tile, const PrTile& T) {
+        const int n_tail = kPrKeys - T.n_valid;
+        if (n_tail <= 0 && T.n_head <= 0) return;
+        if (n_tail > 0) {
+            for (int idx = lane; idx < 2 * n_tail * 8; idx += 32) {
+                const int blk = idx / (n_tail * 8), rem = idx - blk * n_tail * 8;
+                *reinterpret_cast<uint4*>(tile + blk * 2 * kPrBox + (T.n_valid + rem / 8) * 128 +
+                                          (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (T.n_head > 0) {
+            for (int idx = lane; idx < 2 * T.n_head * 8; idx += 32) {
+                const int blk = idx / (T.n_head * 8), rem = idx - blk * T.n_head * 8;
+                *reinterpret_cast<uint4*>(tile + blk * 2 * kPrBox + (rem / 8) * 128 +
+                                          (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    };
+
+    if (warp == kPrProducerWarp) {
+        // ------------------------------- TMA producer --------------------------------------
+        // Loads in the MMA order: K(0), K(1), V(0), K(2), V(1), ... A slot is reused once the
+        // MMAs that read its previous contents have completed.
+        if (lane == 0) {
+            bool ok = true;
+            int L = 0;
+            auto place = [&](const PrTile& T, int key, int& row3, int& slot0) {
+                if (!kv_place(p, T.b, T.kvh, key, row3, slot0)) {
+                    report(p.err, GEMMA_DEVERR_PAGE);  // a bad page index reads zeros
+                    row3 = p.n_pages * p.n_kv;
+                }
+            };
+            auto load = [&](const PrTile& T, bool is_v) {
+                const int s = L % kPrSlots, use = L / kPrSlots;
+                ++L;
+                if (use > 0 && ok) ok = mbar_wait(&empty[s], (use - 1) & 1, p.err);
+                mbar_arrive_expect_tx(&full[s], kPrSlot);
+                if (!ok) return;
+                uint8_t* dst = slots + s * kPrSlot;
+                int row3 = 0, slot0 = 0;
+                if (!is_v) {
+                    // K: this CTA's 64 keys, the four 64-column boxes of head_dim
+                    place(T, T.key0 + 64 * (int)c, row3, slot0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tma_load_3d(dst + j * kPrBox, &kmap, 64 * j, slot0, row3, &full[s]);
+                } else {
+                    // V: this CTA's 128 columns (two blocks of 64) of all 128 keys; block b
+                    // holds keys 0-127 as 128-byte rows, the two 64-key groups one after another
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        place(T, T.key0 + 64 * g, row3, slot0);
+#pragma unroll
+                        for (int blk = 0; blk < 2; ++blk)
+                            tma_load_3d(dst + blk * 2 * kPrBox + g * kPrBox, &vmap,
+                                        128 * (int)c + 64 * blk, slot0, row3, &full[s]);
+                    }
+                }
+            };
+            PrTileIter it;
+            it.init(fp, worker);
+            PrTile prev;
+            prev.valid = false;
+            for (;;) {
+                const PrTile cur = it.next(fp);
+                if (!cur.valid && !prev.valid) break;
+                if (cur.valid) load(cur, false);
+                if (prev.valid) load(prev, true);
+                prev = cur;
+            }
+            // the last releases of the slots (arrivals of the MMA commits on this CTA's
+            // barriers) have landed before the CTA may exit
+            for (int k = 1; k <= kPrSlots && k <= L; ++k) {
+                const int LL = L - k;
+                if (ok) ok = mbar_wait(&empty[LL % kPrSlots], (LL / kPrSlots) & 1, p.err);
+            }
+        }
+    } else if (c == 0 && (warp == kPrSWarp || warp == kPrPvWarp)) {
+        // ------------------ MMA issuers: S (warp 9) and P V (warp 10) -----------------------
+        // An MMA is accepted only when the one before it is nearly done, so an issuing thread
+        // is busy for about the tensor time of what it issues. With S and P V from separate
+        // threads, one issuer's waits (for P, or for the softmax to have read S) leave the
+        // tensor core to the other's MMAs. Both walk the producer's slot order.
+        const bool is_s = warp == kPrSWarp;
+        const uint32_t id_s = idesc_bf16(256, kPrKeys, 0, 0);
+        const uint32_t id_pv = idesc_bf16(256, kPrD, 0, 1);
+        const uint32_t tQ = tmem + kPrQCol, tS = tmem + kPrSCol, tO = tmem + kPrOCol;
+        bool ok = true;
+        int L = 0;
+        // the next slot with both CTAs' halves landed (V: its edge rows zeroed here)
+        auto take = [&](const PrTile& T, bool is_v) -> int {
+            const int s = L % kPrSlots;
+            const uint32_t ph = (L / kPrSlots) & 1;
+            ++L;
+            if (ok) ok = mbar_wait(&full[s], ph, p.err);
+            if (is_v) zero_v(slots + s * kPrSlot, T);
+            if (ok) ok = mbar_wait(&pfull[s], ph, p.err);
+            return s;
+        };
+        PrTileIter it;
+        it.init(fp, worker);
+        PrTile prev;
+        prev.valid = false;
+        int Tn = 0;  // index of `cur` in the flat tile sequence
+        for (;;) {
+            const PrTile cur = it.next(fp);
+            if (!cur.valid && !prev.valid) break;
+            if (cur.valid && !is_s) {
+                ++L;  // K(Tn): the S issuer's
+            } else if (cur.valid) {
+                // S(Tn) = Q K(Tn)^T, once both CTAs' softmax warps have read S(Tn - 1)
+                const int sk = take(cur, false);
+                if (cur.first && ok) ok = mbar_wait(q_ready, cur.ord & 1, p.err);
+                if (Tn > 0 && ok) ok = mbar_wait(s_free, (Tn - 1) & 1, p.err);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t kd = smem_desc_sw128(smem_u32(slots + sk * kPrSlot), 0, 1024);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            umma_ts_pair(tS, tQ + j * 32 + ks * 8,
+                                         kd + (uint64_t)((j * kPrBox + ks * 32) >> 4), id_s,
+                                         (j | ks) ? 1u : 0u);
+                    umma_commit_pair(s_full);
+                    umma_commit_pair(&empty[sk]);
+                }
+                __syncwarp();
+            }
+            if (prev.valid && is_s) {
+                ++L;  // V(Tn - 1): the P V issuer's
+            } else if (prev.valid) {
+                // O (+)= P(Tn - 1) V(Tn - 1)
+                const int Tp = Tn - 1;
+                const int sv = take(prev, true);
+                if (ok) ok = mbar_wait(p_full, Tp & 1, p.err);
+                // a unit's first P V overwrites O: the previous unit's epilogues have read it
+                if (prev.first && prev.ord > 0 && ok)
+                    ok = mbar_wait(o_free, (prev.ord - 1) & 1, p.err);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t vd =
+                        smem_desc_sw128(smem_u32(slots + sv * kPrSlot), 2 * kPrBox, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kPrKeys / 16; ++kk) {
+                        const uint64_t pd = smem_desc_sw128(
+                            smem_u32(sP + (kk >> 2) * (kPrPTile / 2) + (kk & 3) * 32), 0, 1024);
+                        umma_ss_pair(tO, pd, vd + (uint64_t)((kk * 2048) >> 4), id_pv,
+                                     (prev.first && kk == 0) ? 0u : 1u);
+                    }
+                    umma_commit_pair(pv_done);
+                    umma_commit_pair(&empty[sv]);
+                    if (prev.last) umma_commit_pair(o_full);
+                }
+                __syncwarp();
+            }
+            if (cur.valid) ++Tn;
+            prev = cur;
+        }
+    } else if (c == 1 && warp == kPrSWarp) {
+        // ------------------- odd CTA: forwards its slots' arrivals ---------------------------
+        bool ok = true;
+        int L = 0;
+        const uint32_t pfull0 = map_to_peer(&pfull[0], 0);
+        auto fwd = [&](const PrTile& T, bool is_v) {
+            const int s = L % kPrSlots;
+            const uint32_t ph = (L / kPrSlots) & 1;
+            ++L;
+            if (ok) ok = mbar_wait(&full[s], ph, p.err);
+            if (is_v) zero_v(slots + s * kPrSlot, T);
+            if (lane == 0) mbar_arrive_remote(pfull0 + 8u * (uint32_t)s);
+            __syncwarp();
+        };
+        PrTileIter it;
+        it.init(fp, worker);
+        PrTile prev;
+        prev.valid = false;
+        for (;;) {
+            const PrTile cur = it.next(fp);
+            if (!cur.valid && !prev.valid) break;
+            if (cur.valid) fwd(cur, false);
+            if (prev.valid) fwd(prev, true);
+            prev = cur;
+        }
+    } else if (warp < 8) {
+        // ------------------------------ softmax warps --------------------------------------
+        const int w = warp >> 2;          // softmax group: S columns 64w.., O columns 128w..
+        const int r = threadIdx.x & 127;  // tile row = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tSw = tmem + kPrSCol + 64 * w + lane_off;
+        const uint32_t tOw = tmem + kPrOCol + 128 * w + lane_off;
+        const uint32_t tQw = tmem + kPrQCol + 64 * w + lane_off;
+        const uint32_t s_free0 = map_to_peer(s_free, 0), p_full0 = map_to_peer(p_full, 0),
+                       o_free0 = map_to_peer(o_free, 0), q_ready0 = map_to_peer(q_ready, 0);
+        uint8_t* sPw = sP + w * (kPrPTile / 2);  // this group's 64 keys of P
+        bool ok = true;
+
+        auto rows_here = [&](const PrUnit& U) { return max(0, min(128, U.n_rows - 128 * (int)c)); };
+        auto real_here = [&](const PrUnit& U) {
+            return max(0, min(128, U.n_rows_real - 128 * (int)c));
+        };
+        // this group's 128 output columns of row rr of this CTA's rows
+        auto out_row = [&](const PrUnit& U, int rr) -> uint4* {
+            const int R = U.row0 + 128 * (int)c + rr;
+            const int tk = R / p.G, hd = U.kvh * p.G + (R - tk * p.G);
+            return reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                            (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)kPrD +
+                                            128 * w);
+        };
+        auto zero_unit = [&](const PrUnit& U) {  // a unit without tiles: zeros
+            if (r < rows_here(U)) {
+                uint4* o = out_row(U, r);
+#pragma unroll 4
+                for (int j = 0; j < 16; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (U.bad && w == 0 && r == 0 && U.kvh == 0 && U.rt == 0 && c == 0)
+                report(p.err, U.bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
+        };
+        // this group's 128 columns of the unit's Q rows into TMEM (once the previous unit's last
+        // S has completed, which the caller has waited for)
+        auto load_q = [&](const PrUnit& U) {
+            const bool row_ok = r < real_here(U);
+            const int R = U.row0 + 128 * (int)c + (row_ok ? r : 0);
+            const int tk = R / p.G, hd = U.kvh * p.G + (R - tk * p.G);
+            const uint4* qrow = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)kPrD + 128 * w);
+            uint4 qv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) qv[j] = row_ok ? __ldg(qrow + j) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint32_t v[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    v[4 * e + 0] = qv[8 * j + e].x;
+                    v[4 * e + 1] = qv[8 * j + e].y;
+                    v[4 * e + 2] = qv[8 * j + e].z;
+                    v[4 * e + 3] = qv[8 * j + e].w;
+                }
+                tmem_st32(tQw + j * 32, v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(q_ready0);
+        };
+        int u = worker - fp.n_pairs;
+        // finds the next unit with tiles (writing zeros for units without), or returns false
+        auto next_tiled = [&](PrUnit& U) -> bool {
+            for (;;) {
+                u += fp.n_pairs;
+                if (u >= fp.n_units) return false;
+                U = pr_unit(fp, u);
+                if (U.n_tiles > 0) return true;
+                zero_unit(U);
+            }
+        };
+
+        PrUnit cur;
+        if (next_tiled(cur)) {
+            int T_base = 0, ord = 0;
+            load_q(cur);
+            for (;;) {
+                const int lo_pos = cur.len - cur.n_real;  // position of the unit's token 0
+                int lo = 1, hi = 0;
+                if (r < real_here(cur)) {
+                    const int pos = lo_pos + (cur.row0 + 128 * (int)c + r) / p.G;
+                    lo = p.is_sliding ? max(0, pos - p.window + 1) : 0;
+                    hi = pos + 1;
+                }
+                // the next unit's Q rows towards L2 while this unit runs
+                if (cur.n_tiles > 2) {
+                    const int u2 = u + fp.n_pairs;
+                    if (u2 < fp.n_units) {
+                        const PrUnit U2 = pr_unit(fp, u2);
+                        if (r < real_here(U2)) {
+                            const int R = U2.row0 + 128 * (int)c + r;
+                            const int tk = R / p.G, hd = U2.kvh * p.G + (R - tk * p.G);
+                            const char* qrow = reinterpret_cast<const char*>(
+                                reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                (((size_t)U2.b * p.n_tok + tk) * p.n_q + hd) * (size_t)kPrD + 128 * w);
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow));
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + 128));
+                        }
+                    }
+                }
+                float m = -INFINITY, l_w = 0.f;  // l_w: this group's columns, relative to m
+                for (int t = 0; t < cur.n_tiles; ++t) {
+                    const int T = T_base + t;
+                    // ---- this group's 64 columns of S(T) ----
+                    if (ok) ok = mbar_wait(s_full, T & 1, p.err);
+                    tc_fence_after();
+                    float s[64];
+                    {
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(tSw, v0);
+                        tmem_ld32(tSw + 32, v1);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            s[e] = __uint_as_float(v0[e]);
+                            s[32 + e] = __uint_as_float(v1[e]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(s_free0);  // S(T + 1) may overwrite it
+
+                    // scores stay raw; scale > 0, so max(raw) * scale_log2 is the max of the
+                    // scaled scores. With a soft-cap they are first mapped to c * tanh(scale *
+                    // raw / c) in log2 units (before the mask, so masked keys stay -inf), with
+                    // tanh(x) = 1 - 2 / (e^(2x) + 1).
+                    float sl2 = p.scale_log2;
+                    if (SOFTCAP) {
+                        const float k2 = 2.8853900817779268f * p.cap_inner;  // 2 log2(e) s / c
+                        const float c2 = 2.f * p.cap_log2;
+                        const unsigned long long k2x2 = f32x2(k2, k2), zero2 = f32x2(0.f, 0.f),
+                                                 one2 = f32x2(1.f, 1.f), mc2 = f32x2(-c2, -c2),
+                                                 cl2 = f32x2(p.cap_log2, p.cap_log2);
+#pragma unroll
+                        for (int e = 0; e < 64; e += 2) {
+                            const float2 a = f32x2_split(fma_f32x2(f32x2(s[e], s[e + 1]), k2x2, zero2));
+                            const float2 b = f32x2_split(
+                                add_f32x2(f32x2(fast_exp2(a.x), fast_exp2(a.y)), one2));
+                            const float2 o = f32x2_split(
+                                fma_f32x2(mc2, f32x2(fast_rcp(b.x), fast_rcp(b.y)), cl2));
+                            s[e] = o.x;
+                            s[e + 1] = o.y;
+                        }
+                        sl2 = 1.f;
+                    }
+                    const int kt0 = cur.k_begin + t * kPrKeys + 64 * w;
+                    if (!(kt0 >= lo && kt0 + 64 <= hi)) {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) {
+                            const int key = kt0 + e;
+                            if (key < lo || key >= hi) s[e] = -INFINITY;
+                        }
+                    }
+                    float mx8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3f(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+                    for (int e = 24; e < 56; e += 16)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx8[i] = fmax3f(mx8[i], s[e + i], s[e + 8 + i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[56 + i]);
+                    float mx = fmax3f(fmax3f(mx8[0], mx8[1], mx8[2]), fmax3f(mx8[3], mx8[4], mx8[5]),
+                                      fmaxf(mx8[6], mx8[7])) *
+                               sl2;
+                    // ---- the row's maximum over both groups' columns ----
+                    float* mxb = mxs + (T & 1) * 256;
+                    mxb[w * 128 + r] = mx;
+                    named_bar_sync(1, 256);
+                    mx = fmaxf(mx, mxb[(w ^ 1) * 128 + r]);
+                    // ---- the row's reference: moves only by more than 2^8 ----
+                    const float m_prev = m;
+                    const float m_new = mx > m_prev + kPrLazyLog2 ? mx : m_prev;
+                    if (m_new != m_prev) {  // references only grow; l_w follows
+                        l_w = m_prev == -INFINITY ? 0.f : l_w * exp2f(m_prev - m_new);
+                        m = m_new;
+                    }
+                    // ---- O rows whose reference moved: rescale after P V(T-1) ----
+                    // (a row whose earlier keys were all masked has O = 0: nothing to rescale)
+                    const bool resc = t > 0 && m_new != m_prev && m_prev != -INFINITY;
+                    bool pv_waited = false;
+                    if (__any_sync(0xffffffffu, resc)) {
+                        if (ok) ok = mbar_wait(pv_done, (T - 1) & 1, p.err);
+                        pv_waited = true;
+                        tc_fence_after();
+                        const float alpha = resc ? exp2f(m_prev - m_new) : 1.f;
+                        const unsigned long long alpha2 = f32x2(alpha, alpha);
+#pragma unroll 1
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t v[32];
+                            tmem_ld32(tOw + j * 32, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const float2 o = f32x2_split(mul_f32x2(
+                                    f32x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), alpha2));
+                                v[e] = __float_as_uint(o.x);
+                                v[e + 1] = __float_as_uint(o.y);
+                            }
+                            tmem_st32(tOw + j * 32, v);
+                        }
+                        tmem_st_wait();
+                    }
+                    // ---- P(T) = 2^(s * scale_log2 - m), this group's 64 keys ----
+                    const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
+                    const unsigned long long sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
+                    unsigned long long sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+                    uint32_t pw[32];
+#pragma unroll
+                    for (int k2 = 0; k2 < 32; ++k2) {
+                        const float2 x = f32x2_split(fma_f32x2(f32x2(s[2 * k2], s[2 * k2 + 1]), sl2x2, negm2));
+                        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                        sum2[k2 & 1] = add_f32x2(sum2[k2 & 1], f32x2(p0, p1));
+                        pw[k2] = pack_bf16(p0, p1);
+                    }
+                    const float2 sa = f32x2_split(sum2[0]), sb = f32x2_split(sum2[1]);
+                    l_w += (sa.x + sa.y) + (sb.x + sb.y);
+                    // the P buffer is free once P V(T-1) has completed
+                    if (T > 0 && !pv_waited && ok) ok = mbar_wait(pv_done, (T - 1) & 1, p.err);
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc)
+                        *reinterpret_cast<uint4*>(sPw + r * 128 + ((cc ^ (r & 7)) * 16)) =
+                            make_uint4(pw[4 * cc], pw[4 * cc + 1], pw[4 * cc + 2], pw[4 * cc + 3]);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(p_full0);
+                }
+
+                // ---- next unit: its Q rows (S of this unit's last tile has completed) ----
+                PrUnit nxt;
+                const bool more = next_tiled(nxt);
+                if (more) load_q(nxt);
+
+                // ---- epilogue: O / l -> bf16 for this group's 128 columns ----
+                const int T_last = T_base + cur.n_tiles - 1;
+                if (ok) ok = mbar_wait(o_full, ord & 1, p.err);
+                if (ok) ok = mbar_wait(pv_done, T_last & 1, p.err);
+                tc_fence_after();
+                lxs[w * 128 + r] = l_w;
+                named_bar_sync(2, 256);
+                const float lt = l_w + lxs[(w ^ 1) * 128 + r];
+                const float inv = (cur.bad || !(lt > 0.f)) ? 0.f : 1.f / lt;
+                const unsigned long long inv2 = f32x2(inv, inv);
+                // in slices of 64 columns: each thread converts its row's slice to bf16 in this
+                // group's half of the P buffer (free: the unit's last P V has completed), then
+                // each warp writes its 32 rows' slices as whole 128-byte lines
+                uint8_t* stage = sPw;
+                const int wrow0 = (warp & 3) * 32;
+                const int n_here = rows_here(cur);
+#pragma unroll 1
+                for (int sl = 0; sl < 2; ++sl) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        uint32_t v[32];
+                        tmem_ld32(tOw + sl * 64 + j * 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int cc = j * 4 + e;
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float2 o = f32x2_split(mul_f32x2(
+                                    f32x2(__uint_as_float(v[8 * e + 2 * q]), __uint_as_float(v[8 * e + 2 * q + 1])),
+                                    inv2));
+                                w4[q] = pack_bf16(o.x, o.y);
+                            }
+                            *reinterpret_cast<uint4*>(stage + r * 128 + ((cc ^ (r & 7)) * 16)) =
+                                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int it2 = 0; it2 < 8; ++it2) {
+                        const int idx = it2 * 32 + lane;
+                        const int rr = wrow0 + idx / 8, cc = idx % 8;
+                        const uint4 val =
+                            *reinterpret_cast<const uint4*>(stage + rr * 128 + ((cc ^ (rr & 7)) * 16));
+                        if (rr < n_here) out_row(cur, rr)[sl * 8 + cc] = val;
+                    }
+                    __syncwarp();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(o_free0);
+                if (!more) break;
+                T_base += cur.n_tiles;
+                cur = nxt;
+                ++ord;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // neither CTA writes into the other's shared memory or barriers any more
+    if (warp == kPrSWarp) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+cudaError_t launch_prefill_pair(const RowsParams& p, int batch, cudaStream_t st) {
+    CUtensorMap km, vm;
+    // [rows][slots][D]: rows = sequences x KV heads (pages x KV heads for a paged pool)
+    const uint64_t map_slots = p.page_size ? (uint64_t)p.page_size : (uint64_t)p.cap;
+    const uint64_t map_rows = p.page_size ? (uint64_t)p.n_pages * p.n_kv : (uint64_t)batch * p.n_kv;
+    const uint64_t dims[3] = {(uint64_t)kPrD, map_slots, map_rows};
+    const uint64_t strides[2] = {(uint64_t)kPrD * 2, map_slots * kPrD * 2};
+    const uint32_t box[3] = {64, 64, 1};
+    if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+
+    // per device: the shared-memory attribute, and how many pairs fit at once
+    static std::atomic<int> pairs[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    int n_pairs = dev >= 0 && dev < 64 ? pairs[dev].load(std::memory_order_relaxed) : 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(kPrThreads);
+    cfg.dynamicSmemBytes = kPrSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (n_pairs <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPrSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_pair_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kPrSmem);
+        if (e != cudaSuccess) return e;
+        int n_sm = 0;
+        e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        n_pairs = n_sm / 2;
+        cudaLaunchConfig_t occ = cfg;
+        occ.gridDim = dim3(2 * n_pairs);
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, prefill_pair_kernel<false>, &occ);
+        if (e != cudaSuccess) return e;
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        if (clusters < n_pairs) n_pairs = clusters;
+        if (dev >= 0 && dev < 64) pairs[dev].store(n_pairs, std::memory_order_relaxed);
+    }
+    PrParams fp;
+    fp.p = p;
+    fp.batch = batch;
+    fp.n_rt = (p.n_tok * p.G + kPrRows - 1) / kPrRows;
+    fp.n_units = fp.n_rt * batch * p.n_kv;
+    fp.n_pairs = fp.n_units < n_pairs ? fp.n_units : n_pairs;
+    cfg.gridDim = dim3(2 * fp.n_pairs);
+    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<true>, km, vm, fp)
+                           : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<false>, km, vm, fp);
+}
+
+}  // namespace gemma

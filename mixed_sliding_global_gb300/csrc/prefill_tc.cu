@@ -91,22 +91,6 @@ struct FaParams {
     int n_workers; // CTAs (clusters) walking the units
 };
 
-// ---------------------------------------------------------------------------------------------
-// cluster helpers (distributed shared memory between the two CTAs of a cluster)
-// ---------------------------------------------------------------------------------------------
-GEMMA_DEVINL uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-GEMMA_DEVINL void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-GEMMA_DEVINL uint32_t map_to_peer(const void* local, uint32_t peer) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(peer));
-    return r;
-}
 // two fp32 -> packed fp16 (lo in the low half), round to nearest; values beyond the fp16
 // range saturate to +-65504 instead of becoming infinite
 GEMMA_DEVINL uint32_t pack_f16_sat(float lo, float hi) {
@@ -147,12 +131,6 @@ GEMMA_DEVINL void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 GEMMA_DEVINL void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
-}
-// 1 / x (hardware approximation; 1 / +inf = +0)
-GEMMA_DEVINL float fast_rcp(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -936,7 +914,7 @@ cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cuda
     switch (head_dim) {
         case 64: return launch_d<64, 1>(p, batch, st);
         case 128: return launch_d<128, 1>(p, batch, st);
-        case 256: return launch_d<256, 1>(p, batch, st);
+        case 256: return launch_prefill_pair(p, batch, st);
         case 512: return launch_d<512, 2>(p, batch, st);
     }
     return cudaErrorInvalidValue;

@@ -66,6 +66,34 @@ GEMMA_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;"
 GEMMA_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------------------------
+// thread-block clusters (distributed shared memory between the CTAs of a cluster)
+// ---------------------------------------------------------------------------------------------
+GEMMA_DEVINL uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+GEMMA_DEVINL void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// shared::cluster address of `local`'s counterpart in CTA `rank` of the cluster
+GEMMA_DEVINL uint32_t map_to_peer(const void* local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+// Arrival on an mbarrier of any CTA of the cluster (shared::cluster address).
+GEMMA_DEVINL void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// 1 / x (hardware approximation; 1 / +inf = +0)
+GEMMA_DEVINL float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------------------------------------
 // MMA descriptors
 // ---------------------------------------------------------------------------------------------
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation, dense.
@@ -111,6 +139,54 @@ GEMMA_DEVINL void umma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// CTA pairs (cta_group::2): the two CTAs of a 2-CTA cluster run one MMA of M = 256 together.
+// A kernel uses either these forms or the single-CTA forms above, never both.
+// ---------------------------------------------------------------------------------------------
+// One full warp in each CTA of the pair executes it; the same columns are allocated in both
+// CTAs' tensor memory and the base address is written to each CTA's `dst`.
+GEMMA_DEVINL void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+GEMMA_DEVINL void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+GEMMA_DEVINL void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// Issued by one thread of the even CTA. Rows 0-127 of A and D live in the even CTA, rows
+// 128-255 in the odd one (same TMEM columns / shared-memory offsets); B's N columns are split
+// in halves, the first half in the even CTA's shared memory, the second in the odd CTA's.
+GEMMA_DEVINL void umma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+GEMMA_DEVINL void umma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` (the same shared-memory offset) in both CTAs of the pair when every
+// tcgen05 operation this thread issued so far has completed.
+GEMMA_DEVINL void umma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)3)
         : "memory");
 }
 
