@@ -9,9 +9,8 @@
 // Gemma-4 size have head_dim 256.
 //
 // A cluster of two CTAs (one per SM) runs each MMA as one instruction of M = 256: CTA c owns
-// rows 128c..128c+127 of the tile (its Q rows in its tensor memory, its rows of S and O in its
-// tensor memory, its rows of P in its shared memory), and each CTA holds half of every B
-// operand. Per 128-key tile:
+// rows 128c..128c+127 of the tile (its Q rows in its shared memory, its rows of S, P and O in
+// its tensor memory), and each CTA holds half of every B operand. Per 128-key tile:
 //   S = Q K^T   N = 128 keys: CTA c holds keys 64c..64c+63 of K (all 256 columns, 32 KB);
 //   O += P V    N = 256 columns: CTA c holds columns 128c..128c+127 of V (all 128 keys, 32 KB).
 // So a 128-key step needs 64 KB of shared memory per SM (a one-SM 128-key step needs 128 KB),
@@ -26,21 +25,25 @@
 //               swap their row maxima through shared memory; the row's softmax reference moves
 //               only when a tile maximum exceeds it by more than 2^8 (lazy rescaling keeps the
 //               result exact: the final division uses the same reference), and O rows are
-//               rescaled in TMEM when it moves. P goes to shared memory as bf16.
-//   warp 8      TMA producer: this CTA's halves of the K and V tiles (128-byte swizzle, boxes of
+//               rescaled in TMEM when it moves. P goes to tensor memory as bf16 (two buffers,
+//               so the softmax of tile t+1 does not wait for the P V of tile t).
+//   warp 8      TMA producer: each unit's Q rows (once the previous unit's last S has read the
+//               Q buffer) and this CTA's halves of the K and V tiles (128-byte swizzle, boxes of
 //               64 keys x 64 columns) into a FIFO ring of 32 KB slots, in the MMA order.
 //   warp 9      even CTA: issues S(t) = Q K(t)^T once both CTAs' softmax warps have read S(t-1),
 //               so the softmax of tile t overlaps the P V of tile t-1 and the S of tile t+1.
 //               Odd CTA: forwards each of its ring slots' arrivals to the even CTA's barriers
 //               (an MMA reads both CTAs' halves).
-//   warp 10     even CTA: issues O += P(t) V(t) once both CTAs' P(t) is in shared memory.
+//   warp 10     even CTA: issues O += P(t) V(t) once both CTAs' P(t) is in tensor memory.
 // Barriers that the issuers wait on live in the even CTA and count arrivals from both CTAs;
 // the issuers' commits arrive on the same barrier in both CTAs (multicast). Arrivals from the
-// odd CTA are plain remote arrivals: a thread that wrote shared memory an MMA reads (P, zeroed
-// V rows) orders those writes before the async proxy with a proxy fence first, and one that
-// read or wrote tensor memory fences its tcgen05 operations before the arrival.
-// TMEM (512 columns per CTA): Q (128 columns of packed bf16) at 0, S (128 fp32) at 128, O (256
-// fp32) at 256.
+// odd CTA are plain remote arrivals: a thread that wrote shared memory an MMA reads (zeroed V
+// rows) orders those writes before the async proxy with a proxy fence first, and one that read
+// or wrote tensor memory fences its tcgen05 operations before the arrival.
+// TMEM (512 columns per CTA): S (128 fp32) at 0, P (2 x 64 columns of packed bf16) at 128, O
+// (256 fp32) at 256. Shared memory: the ring (4 slots), Q (64 KB), the epilogue's staging.
+// The Q rows of a 128-row half tile are G consecutive heads of 128 / G consecutive tokens, one
+// TMA box per 64 columns; the kernel needs G to divide 128.
 //
 // The key range of a unit is clamped to [first row's window start, last row's position] before
 // any load; rows of a V tile outside the range are zeroed in shared memory before they enter
@@ -65,13 +68,17 @@ constexpr int kPrKeys = 128;                  // keys per tile (N of S)
 constexpr int kPrRows = 256;                  // rows per unit (M of the pair's MMAs)
 constexpr int kPrBox = 64 * 128;              // TMA box: 64 keys x 64 columns of bf16
 constexpr int kPrSlot = 4 * kPrBox;           // K half (64 keys x 256) or V half (128 x 128)
-constexpr int kPrPTile = 128 * kPrKeys * 2;   // P: 128 rows x 128 keys bf16
-constexpr int kPrSlots = 5;
+constexpr int kPrSlots = 4;
+constexpr int kPrQBytes = 128 * kPrD * 2;     // a CTA's Q rows: 4 boxes of 128 rows x 64 columns
+constexpr int kPrQBox = 128 * 128;            // one of them
+constexpr int kPrStage = 2 * 128 * 64;        // epilogue: 2 groups x 128 rows x 32 columns bf16
 constexpr int kPrSmemLimit = 232448;          // max dynamic shared memory per block
 constexpr float kPrLazyLog2 = 8.f;
-constexpr int kPrQCol = 0, kPrSCol = 128, kPrOCol = 256;  // TMEM columns
-// shared memory: ring, P, row maxima [2 tiles][2 groups][128], row sums [2][128], barriers
-constexpr int kPrBarOff = kPrSlots * kPrSlot + kPrPTile + (2 * 2 * 128 + 2 * 128) * 4;
+constexpr int kPrSCol = 0, kPrPCol = 128, kPrOCol = 256;  // TMEM columns
+// shared memory: ring, Q, staging, row maxima [2 tiles][2 groups][128], row sums [2][128],
+// barriers
+constexpr int kPrBarOff =
+    kPrSlots * kPrSlot + kPrQBytes + kPrStage + (2 * 2 * 128 + 2 * 128) * 4;
 constexpr int kPrSmem = kPrBarOff + 256 + 1024;  // + barriers, + alignment slack
 static_assert(kPrSmem <= kPrSmemLimit, "shared memory budget");
 
@@ -135,6 +142,7 @@ struct PrTile {
     int n_head;    // leading keys zeroed (first tile of an aligned-start unit)
     int key0;      // first key
     int b, kvh;
+    int row0;      // the unit's first row
 };
 
 struct PrTileIter {
@@ -166,6 +174,7 @@ struct PrTileIter {
         T.n_head = t == 0 ? U.n_head : 0;
         T.b = U.b;
         T.kvh = U.kvh;
+        T.row0 = U.row0;
         ++t;
         return T;
     }
@@ -178,7 +187,8 @@ struct PrTileIter {
 template <bool SOFTCAP>
 __global__ void __launch_bounds__(kPrThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const PrParams fp) {
+                        const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap qmap, const PrParams fp) {
     pdl_launch_dependents();
     pdl_wait();  // the previous kernel on the stream (the append of these rows) has completed
     const RowsParams& p = fp.p;
@@ -186,8 +196,9 @@ __global__ void __launch_bounds__(kPrThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* slots = smem;
-    uint8_t* sP = smem + kPrSlots * kPrSlot;                          // [2 key blocks][128][64]
-    float* mxs = reinterpret_cast<float*>(sP + kPrPTile);             // [2][2][128]
+    uint8_t* sQ = smem + kPrSlots * kPrSlot;                          // [4][128][64] bf16
+    uint8_t* sStage = sQ + kPrQBytes;                                 // [2][128][32] bf16
+    float* mxs = reinterpret_cast<float*>(sStage + kPrStage);         // [2][2][128]
     float* lxs = mxs + 2 * 2 * 128;                                   // [2][128]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPrBarOff);
     // ring slot s: full[s] completes when this CTA's half has landed (producer arrival +
@@ -196,14 +207,16 @@ __global__ void __launch_bounds__(kPrThreads, 1)
     uint64_t* full = bars;
     uint64_t* pfull = bars + kPrSlots;
     uint64_t* empty = bars + 2 * kPrSlots;
-    uint64_t* s_full = bars + 3 * kPrSlots;  // S(t) is in TMEM (multicast commit)
-    uint64_t* s_free = s_full + 1;           // even CTA: both CTAs' softmax warps have read S(t)
-    uint64_t* p_full = s_full + 2;           // even CTA: both CTAs' P(t) is in shared memory
-    uint64_t* pv_done = s_full + 3;          // P V(t) has completed (multicast commit)
-    uint64_t* o_full = s_full + 4;           // a unit's last P V has completed (multicast)
-    uint64_t* o_free = s_full + 5;           // even CTA: both epilogues have read O
-    uint64_t* q_ready = s_full + 6;          // even CTA: both CTAs' Q rows are in TMEM
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(s_full + 7);
+    uint64_t* q_full = bars + 3 * kPrSlots;  // this CTA's Q rows of a unit have landed
+    uint64_t* q_pfull = q_full + 1;          // even CTA: the odd CTA's have (forwarded)
+    uint64_t* s_full = q_full + 2;           // S(t) is in TMEM (multicast commit)
+    uint64_t* s_free = q_full + 3;           // even CTA: both CTAs' softmax warps have read S(t)
+    uint64_t* p_full = q_full + 4;           // [2] even CTA: both CTAs' P(t) in TMEM buffer t % 2
+    uint64_t* pv_done = q_full + 6;          // [2] P V(t) has completed (multicast commit)
+    uint64_t* o_full = q_full + 8;           // a unit's last P V has completed (multicast)
+    uint64_t* o_free = q_full + 9;           // even CTA: both epilogues have read O
+    uint64_t* q_free = q_full + 10;          // a unit's last S has completed (multicast commit)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(q_full + 11);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t c = cluster_rank();       // 0: issues the pair's MMAs
     const int worker = blockIdx.x >> 1;
@@ -214,13 +227,17 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             mbar_init(&pfull[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(q_full, 1);
+        mbar_init(q_pfull, 1);
         mbar_init(s_full, 1);
         mbar_init(s_free, 16);  // 8 softmax warps per CTA
-        mbar_init(p_full, 16);
-        mbar_init(pv_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&p_full[i], 16);
+            mbar_init(&pv_done[i], 1);
+        }
         mbar_init(o_full, 1);
         mbar_init(o_free, 16);
-        mbar_init(q_ready, 16);
+        mbar_init(q_free, 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -261,7 +278,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
     if (warp == kPrProducerWarp) {
         // ------------------------------- TMA producer --------------------------------------
         // Loads in the MMA order: K(0), K(1), V(0), K(2), V(1), ... A slot is reused once the
-        // MMAs that read its previous contents have completed.
+        // MMAs that read its previous contents have completed. A unit's Q rows go first, once
+        // the previous unit's last S (the last reader of the Q buffer) has completed.
         if (lane == 0) {
             bool ok = true;
             int L = 0;
@@ -302,19 +320,35 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             it.init(fp, worker);
             PrTile prev;
             prev.valid = false;
+            int Tn = 0;
             for (;;) {
                 const PrTile cur = it.next(fp);
                 if (!cur.valid && !prev.valid) break;
+                if (cur.valid && cur.first) {
+                    // (a barrier of its own: this thread runs tiles ahead of the S MMAs, and a
+                    // parity wait must not be more than one phase ahead of the barrier)
+                    if (cur.ord > 0 && ok) ok = mbar_wait(q_free, (cur.ord - 1) & 1, p.err);
+                    mbar_arrive_expect_tx(q_full, kPrQBytes);
+                    const int tk0 = (cur.row0 + 128 * (int)c) / p.G;  // tokens past n_tok read 0
+                    if (ok) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_4d(sQ + j * kPrQBox, &qmap, 64 * j, cur.kvh * p.G, tk0, cur.b,
+                                        q_full);
+                    }
+                }
                 if (cur.valid) load(cur, false);
                 if (prev.valid) load(prev, true);
+                if (cur.valid) ++Tn;
                 prev = cur;
             }
-            // the last releases of the slots (arrivals of the MMA commits on this CTA's
-            // barriers) have landed before the CTA may exit
+            // the last releases of the slots and of the Q buffer (arrivals of the MMA commits
+            // on this CTA's barriers) have landed before the CTA may exit
             for (int k = 1; k <= kPrSlots && k <= L; ++k) {
                 const int LL = L - k;
                 if (ok) ok = mbar_wait(&empty[LL % kPrSlots], (LL / kPrSlots) & 1, p.err);
             }
+            if (Tn > 0 && ok) ok = mbar_wait(q_free, it.ord & 1, p.err);
         }
     } else if (c == 0 && (warp == kPrSWarp || warp == kPrPvWarp)) {
         // ------------------ MMA issuers: S (warp 9) and P V (warp 10) -----------------------
@@ -325,7 +359,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         const bool is_s = warp == kPrSWarp;
         const uint32_t id_s = idesc_bf16(256, kPrKeys, 0, 0);
         const uint32_t id_pv = idesc_bf16(256, kPrD, 0, 1);
-        const uint32_t tQ = tmem + kPrQCol, tS = tmem + kPrSCol, tO = tmem + kPrOCol;
+        const uint32_t tS = tmem + kPrSCol, tP = tmem + kPrPCol, tO = tmem + kPrOCol;
         bool ok = true;
         int L = 0;
         // the next slot with both CTAs' halves landed (V: its edge rows zeroed here)
@@ -351,20 +385,25 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             } else if (cur.valid) {
                 // S(Tn) = Q K(Tn)^T, once both CTAs' softmax warps have read S(Tn - 1)
                 const int sk = take(cur, false);
-                if (cur.first && ok) ok = mbar_wait(q_ready, cur.ord & 1, p.err);
+                if (cur.first && ok) {
+                    ok = mbar_wait(q_full, cur.ord & 1, p.err);
+                    if (ok) ok = mbar_wait(q_pfull, cur.ord & 1, p.err);
+                }
                 if (Tn > 0 && ok) ok = mbar_wait(s_free, (Tn - 1) & 1, p.err);
                 tc_fence_after();
                 if (lane == 0) {
                     const uint64_t kd = smem_desc_sw128(smem_u32(slots + sk * kPrSlot), 0, 1024);
+                    const uint64_t qd = smem_desc_sw128(smem_u32(sQ), 0, 1024);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            umma_ts_pair(tS, tQ + j * 32 + ks * 8,
+                            umma_ss_pair(tS, qd + (uint64_t)((j * kPrQBox + ks * 32) >> 4),
                                          kd + (uint64_t)((j * kPrBox + ks * 32) >> 4), id_s,
                                          (j | ks) ? 1u : 0u);
                     umma_commit_pair(s_full);
                     umma_commit_pair(&empty[sk]);
+                    if (cur.last) umma_commit_pair(q_free);  // the Q buffer may be reloaded
                 }
                 __syncwarp();
             }
@@ -374,7 +413,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                 // O (+)= P(Tn - 1) V(Tn - 1)
                 const int Tp = Tn - 1;
                 const int sv = take(prev, true);
-                if (ok) ok = mbar_wait(p_full, Tp & 1, p.err);
+                if (ok) ok = mbar_wait(&p_full[Tp & 1], (Tp >> 1) & 1, p.err);
                 // a unit's first P V overwrites O: the previous unit's epilogues have read it
                 if (prev.first && prev.ord > 0 && ok)
                     ok = mbar_wait(o_free, (prev.ord - 1) & 1, p.err);
@@ -383,13 +422,11 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     const uint64_t vd =
                         smem_desc_sw128(smem_u32(slots + sv * kPrSlot), 2 * kPrBox, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kPrKeys / 16; ++kk) {
-                        const uint64_t pd = smem_desc_sw128(
-                            smem_u32(sP + (kk >> 2) * (kPrPTile / 2) + (kk & 3) * 32), 0, 1024);
-                        umma_ss_pair(tO, pd, vd + (uint64_t)((kk * 2048) >> 4), id_pv,
+                    for (int kk = 0; kk < kPrKeys / 16; ++kk)
+                        umma_ts_pair(tO, tP + 64 * (Tp & 1) + 8 * kk,
+                                     vd + (uint64_t)((kk * 2048) >> 4), id_pv,
                                      (prev.first && kk == 0) ? 0u : 1u);
-                    }
-                    umma_commit_pair(pv_done);
+                    umma_commit_pair(&pv_done[Tp & 1]);
                     umma_commit_pair(&empty[sv]);
                     if (prev.last) umma_commit_pair(o_full);
                 }
@@ -412,6 +449,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             if (lane == 0) mbar_arrive_remote(pfull0 + 8u * (uint32_t)s);
             __syncwarp();
         };
+        const uint32_t q_pfull0 = map_to_peer(q_pfull, 0);
         PrTileIter it;
         it.init(fp, worker);
         PrTile prev;
@@ -419,6 +457,11 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         for (;;) {
             const PrTile cur = it.next(fp);
             if (!cur.valid && !prev.valid) break;
+            if (cur.valid && cur.first) {
+                if (ok) ok = mbar_wait(q_full, cur.ord & 1, p.err);
+                if (lane == 0) mbar_arrive_remote(q_pfull0);
+                __syncwarp();
+            }
             if (cur.valid) fwd(cur, false);
             if (prev.valid) fwd(prev, true);
             prev = cur;
@@ -430,10 +473,10 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tSw = tmem + kPrSCol + 64 * w + lane_off;
         const uint32_t tOw = tmem + kPrOCol + 128 * w + lane_off;
-        const uint32_t tQw = tmem + kPrQCol + 64 * w + lane_off;
+        const uint32_t tPw = tmem + kPrPCol + 32 * w + lane_off;  // + 64 * buffer
         const uint32_t s_free0 = map_to_peer(s_free, 0), p_full0 = map_to_peer(p_full, 0),
-                       o_free0 = map_to_peer(o_free, 0), q_ready0 = map_to_peer(q_ready, 0);
-        uint8_t* sPw = sP + w * (kPrPTile / 2);  // this group's 64 keys of P
+                       o_free0 = map_to_peer(o_free, 0);
+        uint8_t* stage = sStage + w * (kPrStage / 2);  // this group's epilogue staging
         bool ok = true;
 
         auto rows_here = [&](const PrUnit& U) { return max(0, min(128, U.n_rows - 128 * (int)c)); };
@@ -457,35 +500,6 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             if (U.bad && w == 0 && r == 0 && U.kvh == 0 && U.rt == 0 && c == 0)
                 report(p.err, U.bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
         };
-        // this group's 128 columns of the unit's Q rows into TMEM (once the previous unit's last
-        // S has completed, which the caller has waited for)
-        auto load_q = [&](const PrUnit& U) {
-            const bool row_ok = r < real_here(U);
-            const int R = U.row0 + 128 * (int)c + (row_ok ? r : 0);
-            const int tk = R / p.G, hd = U.kvh * p.G + (R - tk * p.G);
-            const uint4* qrow = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)kPrD + 128 * w);
-            uint4 qv[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) qv[j] = row_ok ? __ldg(qrow + j) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                uint32_t v[32];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    v[4 * e + 0] = qv[8 * j + e].x;
-                    v[4 * e + 1] = qv[8 * j + e].y;
-                    v[4 * e + 2] = qv[8 * j + e].z;
-                    v[4 * e + 3] = qv[8 * j + e].w;
-                }
-                tmem_st32(tQw + j * 32, v);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(q_ready0);
-        };
         int u = worker - fp.n_pairs;
         // finds the next unit with tiles (writing zeros for units without), or returns false
         auto next_tiled = [&](PrUnit& U) -> bool {
@@ -501,7 +515,6 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         PrUnit cur;
         if (next_tiled(cur)) {
             int T_base = 0, ord = 0;
-            load_q(cur);
             for (;;) {
                 const int lo_pos = cur.len - cur.n_real;  // position of the unit's token 0
                 int lo = 1, hi = 0;
@@ -606,10 +619,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     // ---- O rows whose reference moved: rescale after P V(T-1) ----
                     // (a row whose earlier keys were all masked has O = 0: nothing to rescale)
                     const bool resc = t > 0 && m_new != m_prev && m_prev != -INFINITY;
-                    bool pv_waited = false;
                     if (__any_sync(0xffffffffu, resc)) {
-                        if (ok) ok = mbar_wait(pv_done, (T - 1) & 1, p.err);
-                        pv_waited = true;
+                        if (ok) ok = mbar_wait(&pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, p.err);
                         tc_fence_after();
                         const float alpha = resc ? exp2f(m_prev - m_new) : 1.f;
                         const unsigned long long alpha2 = f32x2(alpha, alpha);
@@ -643,69 +654,61 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     }
                     const float2 sa = f32x2_split(sum2[0]), sb = f32x2_split(sum2[1]);
                     l_w += (sa.x + sa.y) + (sb.x + sb.y);
-                    // the P buffer is free once P V(T-1) has completed
-                    if (T > 0 && !pv_waited && ok) ok = mbar_wait(pv_done, (T - 1) & 1, p.err);
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        *reinterpret_cast<uint4*>(sPw + r * 128 + ((cc ^ (r & 7)) * 16)) =
-                            make_uint4(pw[4 * cc], pw[4 * cc + 1], pw[4 * cc + 2], pw[4 * cc + 3]);
-                    fence_proxy_async_smem();
+                    // P buffer T % 2 is free once P V(T-2) has completed
+                    if (T >= 2 && ok) ok = mbar_wait(&pv_done[T & 1], ((T - 2) >> 1) & 1, p.err);
+                    tc_fence_after();
+                    tmem_st32(tPw + 64 * (T & 1), pw);
+                    tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(p_full0);
+                    if (lane == 0) mbar_arrive_remote(p_full0 + 8u * (uint32_t)(T & 1));
                 }
 
-                // ---- next unit: its Q rows (S of this unit's last tile has completed) ----
                 PrUnit nxt;
                 const bool more = next_tiled(nxt);
-                if (more) load_q(nxt);
 
                 // ---- epilogue: O / l -> bf16 for this group's 128 columns ----
                 const int T_last = T_base + cur.n_tiles - 1;
                 if (ok) ok = mbar_wait(o_full, ord & 1, p.err);
-                if (ok) ok = mbar_wait(pv_done, T_last & 1, p.err);
+                if (ok) ok = mbar_wait(&pv_done[T_last & 1], (T_last >> 1) & 1, p.err);
                 tc_fence_after();
                 lxs[w * 128 + r] = l_w;
                 named_bar_sync(2, 256);
                 const float lt = l_w + lxs[(w ^ 1) * 128 + r];
                 const float inv = (cur.bad || !(lt > 0.f)) ? 0.f : 1.f / lt;
                 const unsigned long long inv2 = f32x2(inv, inv);
-                // in slices of 64 columns: each thread converts its row's slice to bf16 in this
-                // group's half of the P buffer (free: the unit's last P V has completed), then
-                // each warp writes its 32 rows' slices as whole 128-byte lines
-                uint8_t* stage = sPw;
+                // in slices of 32 columns: each thread converts its row's slice to bf16 in this
+                // group's staging rows (64 bytes, 16-byte chunks permuted by row so that a warp's
+                // stores spread over the banks), then each warp writes its 32 rows' slices as
+                // whole 64-byte segments
                 const int wrow0 = (warp & 3) * 32;
                 const int n_here = rows_here(cur);
 #pragma unroll 1
-                for (int sl = 0; sl < 2; ++sl) {
+                for (int sl = 0; sl < 4; ++sl) {
+                    uint32_t v[32];
+                    tmem_ld32(tOw + sl * 32, v);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        uint32_t v[32];
-                        tmem_ld32(tOw + sl * 64 + j * 32, v);
-                        tmem_ld_wait();
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t w4[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int cc = j * 4 + e;
-                            uint32_t w4[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float2 o = f32x2_split(mul_f32x2(
-                                    f32x2(__uint_as_float(v[8 * e + 2 * q]), __uint_as_float(v[8 * e + 2 * q + 1])),
-                                    inv2));
-                                w4[q] = pack_bf16(o.x, o.y);
-                            }
-                            *reinterpret_cast<uint4*>(stage + r * 128 + ((cc ^ (r & 7)) * 16)) =
-                                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 o = f32x2_split(mul_f32x2(
+                                f32x2(__uint_as_float(v[8 * cc + 2 * q]), __uint_as_float(v[8 * cc + 2 * q + 1])),
+                                inv2));
+                            w4[q] = pack_bf16(o.x, o.y);
                         }
+                        *reinterpret_cast<uint4*>(stage + r * 64 + ((cc ^ ((r >> 1) & 3)) * 16)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                     __syncwarp();
 #pragma unroll
-                    for (int it2 = 0; it2 < 8; ++it2) {
+                    for (int it2 = 0; it2 < 4; ++it2) {
                         const int idx = it2 * 32 + lane;
-                        const int rr = wrow0 + idx / 8, cc = idx % 8;
-                        const uint4 val =
-                            *reinterpret_cast<const uint4*>(stage + rr * 128 + ((cc ^ (rr & 7)) * 16));
-                        if (rr < n_here) out_row(cur, rr)[sl * 8 + cc] = val;
+                        const int rr = wrow0 + idx / 4, cc = idx % 4;
+                        const uint4 val = *reinterpret_cast<const uint4*>(
+                            stage + rr * 64 + ((cc ^ ((rr >> 1) & 3)) * 16));
+                        if (rr < n_here) out_row(cur, rr)[sl * 4 + cc] = val;
                     }
                     __syncwarp();
                 }
@@ -739,6 +742,15 @@ cudaError_t launch_prefill_pair(const RowsParams& p, int batch, cudaStream_t st)
     const uint32_t box[3] = {64, 64, 1};
     if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    // Q [B][n_tok][n_q][D]: a box of 64 columns x G heads (of one KV head's group) x 128 / G
+    // tokens is one 128-row half tile
+    CUtensorMap qm;
+    const uint64_t qdims[4] = {(uint64_t)kPrD, (uint64_t)p.n_q, (uint64_t)p.n_tok, (uint64_t)batch};
+    const uint64_t qstrides[3] = {(uint64_t)kPrD * 2, (uint64_t)p.n_q * kPrD * 2,
+                                  (uint64_t)p.n_tok * p.n_q * kPrD * 2};
+    const uint32_t qbox[4] = {64, (uint32_t)p.G, (uint32_t)(128 / p.G), 1};
+    if (p.G < 1 || 128 % p.G != 0 || !encode_bf16_sw128(&qm, p.q, 4, qdims, qstrides, qbox))
+        return cudaErrorInvalidValue;
 
     // per device: the shared-memory attribute, and how many pairs fit at once
     static std::atomic<int> pairs[64];
@@ -785,8 +797,8 @@ cudaError_t launch_prefill_pair(const RowsParams& p, int batch, cudaStream_t st)
     fp.n_units = fp.n_rt * batch * p.n_kv;
     fp.n_pairs = fp.n_units < n_pairs ? fp.n_units : n_pairs;
     cfg.gridDim = dim3(2 * fp.n_pairs);
-    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<true>, km, vm, fp)
-                           : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<false>, km, vm, fp);
+    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<true>, km, vm, qm, fp)
+                           : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<false>, km, vm, qm, fp);
 }
 
 }  // namespace gemma

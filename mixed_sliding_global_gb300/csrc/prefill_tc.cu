@@ -914,7 +914,7 @@ cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cuda
     switch (head_dim) {
         case 64: return launch_d<64, 1>(p, batch, st);
         case 128: return launch_d<128, 1>(p, batch, st);
-        case 256: return launch_prefill_pair(p, batch, st);
+        case 256: return launch_prefill_pair(p, batch, st);  // every supported group divides 128
         case 512: return launch_d<512, 2>(p, batch, st);
     }
     return cudaErrorInvalidValue;

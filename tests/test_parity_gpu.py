@@ -102,6 +102,10 @@ PREFILL_SHAPES = [
     (LayerSpec(GLOBAL, 0, 1, 1, 64, False), 200, [333, 200], 352, None),
     (LayerSpec(SLIDING, 1024, 16, 8, 256, False), 160, [4096, 1500], 4096, None),
     (LayerSpec(SLIDING, 5, 4, 4, 256, True), 70, [90, 71], 96, None),
+    # head_dim 256 runs on CTA pairs: 96 units of 256 rows, more than there are pairs, so a pair
+    # walks several units (each a few 128-key tiles); every output compared
+    (LayerSpec(SLIDING, 256, 4, 2, 256, False), 768, [868, 800, 900, 768, 1000, 850, 790, 880],
+     1024, None),
 ]
 
 
