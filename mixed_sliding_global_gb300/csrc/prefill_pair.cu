@@ -188,7 +188,8 @@ template <bool SOFTCAP>
 __global__ void __launch_bounds__(kPrThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
-                        const __grid_constant__ CUtensorMap qmap, const PrParams fp) {
+                        const __grid_constant__ CUtensorMap qmap,
+                        const __grid_constant__ CUtensorMap omap, const PrParams fp) {
     pdl_launch_dependents();
     pdl_wait();  // the previous kernel on the stream (the append of these rows) has completed
     const RowsParams& p = fp.p;
@@ -677,17 +678,25 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                 const float lt = l_w + lxs[(w ^ 1) * 128 + r];
                 const float inv = (cur.bad || !(lt > 0.f)) ? 0.f : 1.f / lt;
                 const unsigned long long inv2 = f32x2(inv, inv);
-                // in slices of 32 columns: each thread converts its row's slice to bf16 in this
-                // group's staging rows (64 bytes, 16-byte chunks permuted by row so that a warp's
-                // stores spread over the banks), then each warp writes its 32 rows' slices as
-                // whole 64-byte segments
-                const int wrow0 = (warp & 3) * 32;
-                const int n_here = rows_here(cur);
+                // in slices of 32 columns: each thread converts its row's slice to bf16 into this
+                // group's staging rows (64 bytes each, 16-byte chunks placed as the 64-byte TMA
+                // swizzle expects), and the group's first thread stores the slice with one TMA
+                // box (32 columns x G heads x 128 / G tokens; rows past the sequence's tokens
+                // are not written), so no thread waits for global stores
+                const bool issuer_t = r == 0;
+                const int tk0 = (cur.row0 + 128 * (int)c) / p.G;
 #pragma unroll 1
                 for (int sl = 0; sl < 4; ++sl) {
+                    if (issuer_t) bulk_wait_read_all();  // the last slice's store has read `stage`
+                    named_bar_sync(3 + w, 128);
                     uint32_t v[32];
                     tmem_ld32(tOw + sl * 32, v);
                     tmem_ld_wait();
+                    if (sl == 3) {  // O has been read: the next unit's first P V may overwrite it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote(o_free0);
+                    }
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         uint32_t w4[4];
@@ -701,20 +710,13 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                         *reinterpret_cast<uint4*>(stage + r * 64 + ((cc ^ ((r >> 1) & 3)) * 16)) =
                             make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
-                    __syncwarp();
-#pragma unroll
-                    for (int it2 = 0; it2 < 4; ++it2) {
-                        const int idx = it2 * 32 + lane;
-                        const int rr = wrow0 + idx / 4, cc = idx % 4;
-                        const uint4 val = *reinterpret_cast<const uint4*>(
-                            stage + rr * 64 + ((cc ^ ((rr >> 1) & 3)) * 16));
-                        if (rr < n_here) out_row(cur, rr)[sl * 4 + cc] = val;
+                    fence_proxy_async_smem();
+                    named_bar_sync(3 + w, 128);
+                    if (issuer_t) {
+                        tma_store_4d(&omap, stage, 128 * w + 32 * sl, cur.kvh * p.G, tk0, cur.b);
+                        bulk_commit_group();
                     }
-                    __syncwarp();
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(o_free0);
                 if (!more) break;
                 T_base += cur.n_tiles;
                 cur = nxt;
@@ -722,6 +724,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             }
         }
     }
+    if (warp < 8 && (threadIdx.x & 127) == 0) bulk_wait_all();  // the epilogues' TMA stores
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // neither CTA writes into the other's shared memory or barriers any more
@@ -750,6 +753,11 @@ cudaError_t launch_prefill_pair(const RowsParams& p, int batch, cudaStream_t st)
                                   (uint64_t)p.n_tok * p.n_q * kPrD * 2};
     const uint32_t qbox[4] = {64, (uint32_t)p.G, (uint32_t)(128 / p.G), 1};
     if (p.G < 1 || 128 % p.G != 0 || !encode_bf16_sw128(&qm, p.q, 4, qdims, qstrides, qbox))
+        return cudaErrorInvalidValue;
+    // out, the same layout: boxes of 32 columns (64-byte rows, 64-byte swizzle)
+    CUtensorMap om;
+    const uint32_t obox[4] = {32, (uint32_t)p.G, (uint32_t)(128 / p.G), 1};
+    if (!encode_bf16(&om, p.out, 4, qdims, qstrides, obox, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
 
     // per device: the shared-memory attribute, and how many pairs fit at once
@@ -797,8 +805,9 @@ cudaError_t launch_prefill_pair(const RowsParams& p, int batch, cudaStream_t st)
     fp.n_units = fp.n_rt * batch * p.n_kv;
     fp.n_pairs = fp.n_units < n_pairs ? fp.n_units : n_pairs;
     cfg.gridDim = dim3(2 * fp.n_pairs);
-    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<true>, km, vm, qm, fp)
-                           : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<false>, km, vm, qm, fp);
+    return p.softcap > 0.f
+               ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<true>, km, vm, qm, om, fp)
+               : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<false>, km, vm, qm, om, fp);
 }
 
 }  // namespace gemma

@@ -211,4 +211,23 @@ GEMMA_DEVINL void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1,
         : "memory");
 }
 
+// Tiled TMA store from shared memory (bulk async-group completion); the source must have been
+// written through the generic proxy and made visible to the async proxy (fence_proxy_async_smem)
+// by every writing thread before a barrier that this thread passed.
+GEMMA_DEVINL void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                               int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+        : "memory");
+}
+GEMMA_DEVINL void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed bulk store of this thread has finished reading its shared-memory source
+GEMMA_DEVINL void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed bulk store of this thread has completed
+GEMMA_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 }  // namespace gemma
