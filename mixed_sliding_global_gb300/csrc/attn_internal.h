@@ -87,8 +87,9 @@ cudaError_t launch_combine(const RowsParams& p, int head_dim, int batch, int out
                            cudaStream_t st);
 bool prefill_tc_supported(int head_dim);
 cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cudaStream_t st);
-// head_dim 256 on CTA pairs (called by launch_prefill_tc)
-cudaError_t launch_prefill_pair(const RowsParams& p, int batch, cudaStream_t st);
+// head_dim 256 (one CTA pair) or 512 (two pairs, one per half of head_dim) on clusters issuing
+// 2-SM MMAs (called by launch_prefill_tc)
+cudaError_t launch_prefill_pair(const RowsParams& p, int head_dim, int batch, cudaStream_t st);
 // paged pool layout for the append (block_table == nullptr: a plain or ring cache)
 struct PagedLayout {
     const int32_t* block_table;

@@ -58,7 +58,6 @@ namespace gemma {
 
 namespace {
 
-constexpr int kPrD = 256;
 constexpr int kPrWarps = 11;
 constexpr int kPrThreads = kPrWarps * 32;
 constexpr int kPrProducerWarp = 8;
@@ -68,26 +67,35 @@ constexpr int kPrKeys = 128;                  // keys per tile (N of S)
 constexpr int kPrRows = 256;                  // rows per unit (M of the pair's MMAs)
 constexpr int kPrBox = 64 * 128;              // TMA box: 64 keys x 64 columns of bf16
 constexpr int kPrSlot = 4 * kPrBox;           // K half (64 keys x 256) or V half (128 x 128)
-constexpr int kPrSlots = 4;
-constexpr int kPrQBytes = 128 * kPrD * 2;     // a CTA's Q rows: 4 boxes of 128 rows x 64 columns
+constexpr int kPrQBytes = 128 * 256 * 2;      // a CTA's Q rows: 4 boxes of 128 rows x 64 columns
 constexpr int kPrQBox = 128 * 128;            // one of them
 constexpr int kPrStage = 2 * 128 * 64;        // epilogue: 2 groups x 128 rows x 32 columns bf16
 constexpr int kPrSmemLimit = 232448;          // max dynamic shared memory per block
 constexpr float kPrLazyLog2 = 8.f;
 constexpr int kPrSCol = 0, kPrPCol = 128, kPrOCol = 256;  // TMEM columns
-// shared memory: ring, Q, staging, row maxima [2 tiles][2 groups][128], row sums [2][128],
-// barriers
-constexpr int kPrBarOff =
-    kPrSlots * kPrSlot + kPrQBytes + kPrStage + (2 * 2 * 128 + 2 * 128) * 4;
-constexpr int kPrSmem = kPrBarOff + 256 + 1024;  // + barriers, + alignment slack
-static_assert(kPrSmem <= kPrSmemLimit, "shared memory budget");
+// H parts of head_dim (256 columns each): a cluster of H pairs. Shared memory: ring, Q,
+// staging, the partner pair's partial scores (H = 2: [2 groups][8 chunks][128 rows] x 16
+// bytes), row maxima [2 tiles][2 groups][128], row sums [2][128], barriers.
+template <int H>
+struct PrLay {
+    static constexpr int D = 256 * H;                  // head_dim
+    static constexpr int SLOTS = H == 1 ? 4 : 3;       // ring slots
+    static constexpr int Q_OFF = SLOTS * kPrSlot;
+    static constexpr int STAGE_OFF = Q_OFF + kPrQBytes;
+    static constexpr int X_OFF = STAGE_OFF + kPrStage;
+    static constexpr int X_BYTES = H == 2 ? 128 * kPrKeys * 2 : 0;
+    static constexpr int MX_OFF = X_OFF + X_BYTES;
+    static constexpr int BAR_OFF = MX_OFF + (2 * 2 * 128 + 2 * 128) * 4;
+    static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers, + alignment slack
+    static_assert(SMEM <= kPrSmemLimit, "shared memory budget");
+};
 
 struct PrParams {
     RowsParams p;
     int batch;
     int n_rt;      // 256-row tiles per (sequence, KV head)
     int n_units;   // n_rt * batch * n_kv
-    int n_pairs;   // clusters walking the units
+    int n_pairs;   // clusters walking the units (each of H pairs)
 };
 
 struct PrUnit {
@@ -184,7 +192,7 @@ struct PrTileIter {
 
 // SOFTCAP: the soft-capped variant (a separate instantiation, so that the plain kernel carries
 // no code for it)
-template <bool SOFTCAP>
+template <int H, bool SOFTCAP>
 __global__ void __launch_bounds__(kPrThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
@@ -192,16 +200,20 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                         const __grid_constant__ CUtensorMap omap, const PrParams fp) {
     pdl_launch_dependents();
     pdl_wait();  // the previous kernel on the stream (the append of these rows) has completed
+    using Lay = PrLay<H>;
+    constexpr int D = Lay::D;
+    constexpr int kPrSlots = Lay::SLOTS;
     const RowsParams& p = fp.p;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* slots = smem;
-    uint8_t* sQ = smem + kPrSlots * kPrSlot;                          // [4][128][64] bf16
-    uint8_t* sStage = sQ + kPrQBytes;                                 // [2][128][32] bf16
-    float* mxs = reinterpret_cast<float*>(sStage + kPrStage);         // [2][2][128]
+    uint8_t* sQ = smem + Lay::Q_OFF;                                  // [4][128][64] bf16
+    uint8_t* sStage = smem + Lay::STAGE_OFF;                          // [2][128][32] bf16
+    uint8_t* sX = smem + Lay::X_OFF;                                  // H = 2: partner's scores
+    float* mxs = reinterpret_cast<float*>(smem + Lay::MX_OFF);        // [2][2][128]
     float* lxs = mxs + 2 * 2 * 128;                                   // [2][128]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPrBarOff);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFF);
     // ring slot s: full[s] completes when this CTA's half has landed (producer arrival +
     // transaction bytes); pfull[s] (even CTA) when the odd CTA's half has (its warp 9 forwards
     // its own full[s]); empty[s] when the MMAs that read the slot have completed (multicast).
@@ -217,10 +229,16 @@ __global__ void __launch_bounds__(kPrThreads, 1)
     uint64_t* o_full = q_full + 8;           // a unit's last P V has completed (multicast)
     uint64_t* o_free = q_full + 9;           // even CTA: both epilogues have read O
     uint64_t* q_free = q_full + 10;          // a unit's last S has completed (multicast commit)
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(q_full + 11);
+    uint64_t* x_full = q_full + 11;          // [2] H = 2: the partner's scores of group w landed
+    uint64_t* x_free = q_full + 13;          // [2] H = 2: the partner has read what was sent
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(q_full + 15);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t c = cluster_rank();       // 0: issues the pair's MMAs
-    const int worker = blockIdx.x >> 1;
+    const uint32_t rank = cluster_rank();
+    const uint32_t c = rank & 1u;            // row half of the pair's tile; 0 issues its MMAs
+    const uint32_t h = rank >> 1;            // H = 2: head_dim half (columns 256h..256h+255)
+    const uint32_t lead = rank & ~1u;        // the pair's issuing CTA
+    const uint16_t pair_mask = (uint16_t)(3u << lead);
+    const int worker = blockIdx.x / (2 * H);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPrSlots; ++s) {
@@ -239,11 +257,15 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         mbar_init(o_full, 1);
         mbar_init(o_free, 16);
         mbar_init(q_free, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&x_full[i], 1);  // one local arrival with the exchange's byte count
+            mbar_init(&x_free[i], 4);  // the partner's four warps of the group have read it
+        }
         fence_barrier_init();
     }
     __syncthreads();
-    // both CTAs run and their barriers exist before the pair allocation, any remote arrival or
-    // any multicast commit
+    // every CTA of the cluster runs and its barriers exist before the pair allocation, any
+    // remote arrival or any multicast commit
     cluster_sync();
     if (warp == kPrSWarp) {  // one warp in each CTA, together
         tmem_alloc_pair(tslot, 512);
@@ -303,7 +325,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     place(T, T.key0 + 64 * (int)c, row3, slot0);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        tma_load_3d(dst + j * kPrBox, &kmap, 64 * j, slot0, row3, &full[s]);
+                        tma_load_3d(dst + j * kPrBox, &kmap, 256 * (int)h + 64 * j, slot0, row3,
+                                    &full[s]);
                 } else {
                     // V: this CTA's 128 columns (two blocks of 64) of all 128 keys; block b
                     // holds keys 0-127 as 128-byte rows, the two 64-key groups one after another
@@ -313,7 +336,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
 #pragma unroll
                         for (int blk = 0; blk < 2; ++blk)
                             tma_load_3d(dst + blk * 2 * kPrBox + g * kPrBox, &vmap,
-                                        128 * (int)c + 64 * blk, slot0, row3, &full[s]);
+                                        256 * (int)h + 128 * (int)c + 64 * blk, slot0, row3,
+                                        &full[s]);
                     }
                 }
             };
@@ -334,8 +358,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     if (ok) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            tma_load_4d(sQ + j * kPrQBox, &qmap, 64 * j, cur.kvh * p.G, tk0, cur.b,
-                                        q_full);
+                            tma_load_4d(sQ + j * kPrQBox, &qmap, 256 * (int)h + 64 * j,
+                                        cur.kvh * p.G, tk0, cur.b, q_full);
                     }
                 }
                 if (cur.valid) load(cur, false);
@@ -359,7 +383,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         // tensor core to the other's MMAs. Both walk the producer's slot order.
         const bool is_s = warp == kPrSWarp;
         const uint32_t id_s = idesc_bf16(256, kPrKeys, 0, 0);
-        const uint32_t id_pv = idesc_bf16(256, kPrD, 0, 1);
+        const uint32_t id_pv = idesc_bf16(256, 256, 0, 1);
         const uint32_t tS = tmem + kPrSCol, tP = tmem + kPrPCol, tO = tmem + kPrOCol;
         bool ok = true;
         int L = 0;
@@ -402,9 +426,9 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                             umma_ss_pair(tS, qd + (uint64_t)((j * kPrQBox + ks * 32) >> 4),
                                          kd + (uint64_t)((j * kPrBox + ks * 32) >> 4), id_s,
                                          (j | ks) ? 1u : 0u);
-                    umma_commit_pair(s_full);
-                    umma_commit_pair(&empty[sk]);
-                    if (cur.last) umma_commit_pair(q_free);  // the Q buffer may be reloaded
+                    umma_commit_pair(s_full, pair_mask);
+                    umma_commit_pair(&empty[sk], pair_mask);
+                    if (cur.last) umma_commit_pair(q_free, pair_mask);  // the Q buffer may be reloaded
                 }
                 __syncwarp();
             }
@@ -427,9 +451,9 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                         umma_ts_pair(tO, tP + 64 * (Tp & 1) + 8 * kk,
                                      vd + (uint64_t)((kk * 2048) >> 4), id_pv,
                                      (prev.first && kk == 0) ? 0u : 1u);
-                    umma_commit_pair(&pv_done[Tp & 1]);
-                    umma_commit_pair(&empty[sv]);
-                    if (prev.last) umma_commit_pair(o_full);
+                    umma_commit_pair(&pv_done[Tp & 1], pair_mask);
+                    umma_commit_pair(&empty[sv], pair_mask);
+                    if (prev.last) umma_commit_pair(o_full, pair_mask);
                 }
                 __syncwarp();
             }
@@ -440,7 +464,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         // ------------------- odd CTA: forwards its slots' arrivals ---------------------------
         bool ok = true;
         int L = 0;
-        const uint32_t pfull0 = map_to_peer(&pfull[0], 0);
+        const uint32_t pfull0 = map_to_peer(&pfull[0], lead);
         auto fwd = [&](const PrTile& T, bool is_v) {
             const int s = L % kPrSlots;
             const uint32_t ph = (L / kPrSlots) & 1;
@@ -450,7 +474,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             if (lane == 0) mbar_arrive_remote(pfull0 + 8u * (uint32_t)s);
             __syncwarp();
         };
-        const uint32_t q_pfull0 = map_to_peer(q_pfull, 0);
+        const uint32_t q_pfull0 = map_to_peer(q_pfull, lead);
         PrTileIter it;
         it.init(fp, worker);
         PrTile prev;
@@ -475,8 +499,15 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         const uint32_t tSw = tmem + kPrSCol + 64 * w + lane_off;
         const uint32_t tOw = tmem + kPrOCol + 128 * w + lane_off;
         const uint32_t tPw = tmem + kPrPCol + 32 * w + lane_off;  // + 64 * buffer
-        const uint32_t s_free0 = map_to_peer(s_free, 0), p_full0 = map_to_peer(p_full, 0),
-                       o_free0 = map_to_peer(o_free, 0);
+        const uint32_t s_free0 = map_to_peer(s_free, lead), p_full0 = map_to_peer(p_full, lead),
+                       o_free0 = map_to_peer(o_free, lead);
+        // H = 2: this row's slot in the partner's (rank ^ 2) copy of the exchange buffer
+        uint32_t peer_x = 0, peer_x_full = 0, peer_x_free = 0;
+        if (H == 2) {
+            peer_x = map_to_peer(sX + w * (Lay::X_BYTES / 2) + 16 * r, rank ^ 2u);
+            peer_x_full = map_to_peer(&x_full[w], rank ^ 2u);
+            peer_x_free = map_to_peer(&x_free[w], rank ^ 2u);
+        }
         uint8_t* stage = sStage + w * (kPrStage / 2);  // this group's epilogue staging
         bool ok = true;
 
@@ -489,8 +520,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             const int R = U.row0 + 128 * (int)c + rr;
             const int tk = R / p.G, hd = U.kvh * p.G + (R - tk * p.G);
             return reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                            (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)kPrD +
-                                            128 * w);
+                                            (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D +
+                                            256 * h + 128 * w);
         };
         auto zero_unit = [&](const PrUnit& U) {  // a unit without tiles: zeros
             if (r < rows_here(U)) {
@@ -498,7 +529,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
 #pragma unroll 4
                 for (int j = 0; j < 16; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
             }
-            if (U.bad && w == 0 && r == 0 && U.kvh == 0 && U.rt == 0 && c == 0)
+            if (U.bad && w == 0 && r == 0 && U.kvh == 0 && U.rt == 0 && rank == 0)
                 report(p.err, U.bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
         };
         int u = worker - fp.n_pairs;
@@ -534,7 +565,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                             const int tk = R / p.G, hd = U2.kvh * p.G + (R - tk * p.G);
                             const char* qrow = reinterpret_cast<const char*>(
                                 reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                (((size_t)U2.b * p.n_tok + tk) * p.n_q + hd) * (size_t)kPrD + 128 * w);
+                                (((size_t)U2.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D + 256 * h + 128 * w);
                             asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow));
                             asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + 128));
                         }
@@ -561,6 +592,41 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_remote(s_free0);  // S(T + 1) may overwrite it
+
+                    if (H == 2) {
+                        // S over this pair's half of head_dim: send the partial to the partner
+                        // (asynchronous stores that count bytes on its x_full, fp16 saturating)
+                        // and add the partner's; each side keeps its own partial in fp32
+                        if (r == 0) mbar_arrive_expect_tx(&x_full[w], 128 * 64 * 2);
+                        if (T >= 1 && ok) ok = mbar_wait_cluster(&x_free[w], (T - 1) & 1, p.err);
+                        // chunk-major layout X[c][r] (16-byte chunks of 8 fp16 scores): a warp's
+                        // 32 stores of chunk c are one contiguous 512-byte write
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8)
+                            st_async_v4(peer_x + c8 * (128 * 16), pack_f16_sat(s[8 * c8], s[8 * c8 + 1]),
+                                        pack_f16_sat(s[8 * c8 + 2], s[8 * c8 + 3]),
+                                        pack_f16_sat(s[8 * c8 + 4], s[8 * c8 + 5]),
+                                        pack_f16_sat(s[8 * c8 + 6], s[8 * c8 + 7]), peer_x_full);
+                        if (ok) ok = mbar_wait_cluster(&x_full[w], T & 1, p.err);
+                        const uint4* xr =
+                            reinterpret_cast<const uint4*>(sX + w * (Lay::X_BYTES / 2)) + r;
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const uint4 x = xr[c8 * 128];
+                            const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 f = unpack_f16(wd[i]);
+                                const float2 t2 = f32x2_split(add_f32x2(
+                                    f32x2(s[8 * c8 + 2 * i], s[8 * c8 + 2 * i + 1]), f32x2(f.x, f.y)));
+                                s[8 * c8 + 2 * i] = t2.x;
+                                s[8 * c8 + 2 * i + 1] = t2.y;
+                            }
+                        }
+                        // every lane has consumed its loads of X[w]: the partner may overwrite it
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote_relaxed(peer_x_free);
+                    }
 
                     // scores stay raw; scale > 0, so max(raw) * scale_log2 is the max of the
                     // scaled scores. With a soft-cap they are first mapped to c * tanh(scale *
@@ -713,7 +779,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     fence_proxy_async_smem();
                     named_bar_sync(3 + w, 128);
                     if (issuer_t) {
-                        tma_store_4d(&omap, stage, 128 * w + 32 * sl, cur.kvh * p.G, tk0, cur.b);
+                        tma_store_4d(&omap, stage, 256 * (int)h + 128 * w + 32 * sl, cur.kvh * p.G,
+                                     tk0, cur.b);
                         bulk_commit_group();
                     }
                 }
@@ -727,7 +794,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
     if (warp < 8 && (threadIdx.x & 127) == 0) bulk_wait_all();  // the epilogues' TMA stores
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // neither CTA writes into the other's shared memory or barriers any more
+    cluster_sync();  // no CTA writes into another's shared memory or barriers any more
     if (warp == kPrSWarp) {
         tc_fence_after();
         tmem_dealloc_pair(tmem, 512);
@@ -735,22 +802,25 @@ __global__ void __launch_bounds__(kPrThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-cudaError_t launch_prefill_pair(const RowsParams& p, int batch, cudaStream_t st) {
+template <int H>
+static cudaError_t launch_pair(const RowsParams& p, int batch, cudaStream_t st) {
+    using Lay = PrLay<H>;
+    constexpr int D = Lay::D;
     CUtensorMap km, vm;
     // [rows][slots][D]: rows = sequences x KV heads (pages x KV heads for a paged pool)
     const uint64_t map_slots = p.page_size ? (uint64_t)p.page_size : (uint64_t)p.cap;
     const uint64_t map_rows = p.page_size ? (uint64_t)p.n_pages * p.n_kv : (uint64_t)batch * p.n_kv;
-    const uint64_t dims[3] = {(uint64_t)kPrD, map_slots, map_rows};
-    const uint64_t strides[2] = {(uint64_t)kPrD * 2, map_slots * kPrD * 2};
+    const uint64_t dims[3] = {(uint64_t)D, map_slots, map_rows};
+    const uint64_t strides[2] = {(uint64_t)D * 2, map_slots * D * 2};
     const uint32_t box[3] = {64, 64, 1};
     if (!encode_bf16_sw128(&km, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!encode_bf16_sw128(&vm, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
     // Q [B][n_tok][n_q][D]: a box of 64 columns x G heads (of one KV head's group) x 128 / G
     // tokens is one 128-row half tile
     CUtensorMap qm;
-    const uint64_t qdims[4] = {(uint64_t)kPrD, (uint64_t)p.n_q, (uint64_t)p.n_tok, (uint64_t)batch};
-    const uint64_t qstrides[3] = {(uint64_t)kPrD * 2, (uint64_t)p.n_q * kPrD * 2,
-                                  (uint64_t)p.n_tok * p.n_q * kPrD * 2};
+    const uint64_t qdims[4] = {(uint64_t)D, (uint64_t)p.n_q, (uint64_t)p.n_tok, (uint64_t)batch};
+    const uint64_t qstrides[3] = {(uint64_t)D * 2, (uint64_t)p.n_q * D * 2,
+                                  (uint64_t)p.n_tok * p.n_q * D * 2};
     const uint32_t qbox[4] = {64, (uint32_t)p.G, (uint32_t)(128 / p.G), 1};
     if (p.G < 1 || 128 % p.G != 0 || !encode_bf16_sw128(&qm, p.q, 4, qdims, qstrides, qbox))
         return cudaErrorInvalidValue;
@@ -760,54 +830,60 @@ cudaError_t launch_prefill_pair(const RowsParams& p, int batch, cudaStream_t st)
     if (!encode_bf16(&om, p.out, 4, qdims, qstrides, obox, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
 
-    // per device: the shared-memory attribute, and how many pairs fit at once
-    static std::atomic<int> pairs[64];
+    // per device: the shared-memory attribute, and how many clusters fit at once
+    static std::atomic<int> clusters_fit[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    int n_pairs = dev >= 0 && dev < 64 ? pairs[dev].load(std::memory_order_relaxed) : 0;
+    int n_clusters = dev >= 0 && dev < 64 ? clusters_fit[dev].load(std::memory_order_relaxed) : 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = 2 * H;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kPrThreads);
-    cfg.dynamicSmemBytes = kPrSmem;
+    cfg.dynamicSmemBytes = Lay::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (n_pairs <= 0) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPrSmem);
+    if (n_clusters <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<H, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_pair_kernel<true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kPrSmem);
+            e = cudaFuncSetAttribute(prefill_pair_kernel<H, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
         if (e != cudaSuccess) return e;
         int n_sm = 0;
         e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        n_pairs = n_sm / 2;
+        n_clusters = n_sm / (2 * H);
         cudaLaunchConfig_t occ = cfg;
-        occ.gridDim = dim3(2 * n_pairs);
-        int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, prefill_pair_kernel<false>, &occ);
+        occ.gridDim = dim3(2 * H * n_clusters);
+        int fit = 0;
+        e = cudaOccupancyMaxActiveClusters(&fit, prefill_pair_kernel<H, false>, &occ);
         if (e != cudaSuccess) return e;
-        if (clusters < 1) return cudaErrorInvalidConfiguration;
-        if (clusters < n_pairs) n_pairs = clusters;
-        if (dev >= 0 && dev < 64) pairs[dev].store(n_pairs, std::memory_order_relaxed);
+        if (fit < 1) return cudaErrorInvalidConfiguration;
+        if (fit < n_clusters) n_clusters = fit;
+        if (dev >= 0 && dev < 64) clusters_fit[dev].store(n_clusters, std::memory_order_relaxed);
     }
     PrParams fp;
     fp.p = p;
     fp.batch = batch;
     fp.n_rt = (p.n_tok * p.G + kPrRows - 1) / kPrRows;
     fp.n_units = fp.n_rt * batch * p.n_kv;
-    fp.n_pairs = fp.n_units < n_pairs ? fp.n_units : n_pairs;
-    cfg.gridDim = dim3(2 * fp.n_pairs);
+    fp.n_pairs = fp.n_units < n_clusters ? fp.n_units : n_clusters;
+    cfg.gridDim = dim3(2 * H * fp.n_pairs);
     return p.softcap > 0.f
-               ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<true>, km, vm, qm, om, fp)
-               : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<false>, km, vm, qm, om, fp);
+               ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, true>, km, vm, qm, om, fp)
+               : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, false>, km, vm, qm, om, fp);
+}
+
+cudaError_t launch_prefill_pair(const RowsParams& p, int head_dim, int batch, cudaStream_t st) {
+    if (head_dim == 256) return launch_pair<1>(p, batch, st);
+    if (head_dim == 512) return launch_pair<2>(p, batch, st);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gemma

@@ -91,24 +91,6 @@ struct FaParams {
     int n_workers; // CTAs (clusters) walking the units
 };
 
-// two fp32 -> packed fp16 (lo in the low half), round to nearest; values beyond the fp16
-// range saturate to +-65504 instead of becoming infinite
-GEMMA_DEVINL uint32_t pack_f16_sat(float lo, float hi) {
-    uint32_t d;
-    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-    return d;
-}
-GEMMA_DEVINL float2 unpack_f16(uint32_t v) {
-    __half2 h = *reinterpret_cast<__half2*>(&v);
-    return __half22float2(h);
-}
-// Arrival on the peer CTA's mbarrier without release ordering: used only after loads whose
-// values have already been consumed (so the reads are complete), where a release would also
-// wait for this thread's outstanding asynchronous stores to the peer.
-GEMMA_DEVINL void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
 // Non-blocking check of a phase's completion (cheaper than try_wait when it has completed).
 GEMMA_DEVINL bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
@@ -914,8 +896,8 @@ cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cuda
     switch (head_dim) {
         case 64: return launch_d<64, 1>(p, batch, st);
         case 128: return launch_d<128, 1>(p, batch, st);
-        case 256: return launch_prefill_pair(p, batch, st);  // every supported group divides 128
-        case 512: return launch_d<512, 2>(p, batch, st);
+        case 256: return launch_prefill_pair(p, 256, batch, st);  // every supported group divides 128
+        case 512: return launch_prefill_pair(p, 512, batch, st);
     }
     return cudaErrorInvalidValue;
 }

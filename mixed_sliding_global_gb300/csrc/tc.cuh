@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -85,6 +86,24 @@ GEMMA_DEVINL uint32_t map_to_peer(const void* local, uint32_t rank) {
 // Arrival on an mbarrier of any CTA of the cluster (shared::cluster address).
 GEMMA_DEVINL void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// two fp32 -> packed fp16 (lo in the low half), round to nearest; values beyond the fp16
+// range saturate to +-65504 instead of becoming infinite
+GEMMA_DEVINL uint32_t pack_f16_sat(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+GEMMA_DEVINL float2 unpack_f16(uint32_t v) {
+    __half2 h = *reinterpret_cast<__half2*>(&v);
+    return __half22float2(h);
+}
+// Arrival on the peer CTA's mbarrier without release ordering: used only after loads whose
+// values have already been consumed (so the reads are complete), where a release would also
+// wait for this thread's outstanding asynchronous stores to the peer.
+GEMMA_DEVINL void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
 }
 // 1 / x (hardware approximation; 1 / +inf = +0)
 GEMMA_DEVINL float fast_rcp(float x) {
@@ -180,13 +199,14 @@ GEMMA_DEVINL void umma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// Arrive once on `bar` (the same shared-memory offset) in both CTAs of the pair when every
-// tcgen05 operation this thread issued so far has completed.
-GEMMA_DEVINL void umma_commit_pair(uint64_t* bar) {
+// Arrive once on `bar` (the same shared-memory offset) in the CTAs of `cta_mask` (bit i: cluster
+// rank i; the pair's two CTAs) when every tcgen05 operation this thread issued so far has
+// completed.
+GEMMA_DEVINL void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
         "[%0], %1;" ::"r"(smem_u32(bar)),
-        "h"((uint16_t)3)
+        "h"(cta_mask)
         : "memory");
 }
 
