@@ -6,7 +6,10 @@
 // owner layer ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", sections 2.1-2.3; the
 // pages' "eager" matmul-softmax-matmul definition, section 4.3).
 //
-// Persistent grid: one CTA (head_dim 512: one 2-CTA cluster) per SM walks work units = (row
+// This kernel runs head_dim 64 and 128; head_dim 256 and 512 run on CTA pairs issuing 2-SM
+// MMAs (prefill_pair.cu).
+//
+// Persistent grid: one CTA per SM walks work units = (row
 // tile, sequence, KV head), latest row tiles (longest key ranges) first, and within a unit
 // 64-key tiles. The tiles of all its units form one flat sequence T = 0, 1, 2, ... per CTA.
 // Each CTA has 10 warps:
@@ -29,18 +32,8 @@
 // step. Within a step, each 64-column block of S is preceded by one of the (longer) P V MMAs:
 // the issuing thread shares its SM sub-partition with softmax warps, and a long MMA gives it
 // time to be scheduled before the pipe runs dry.
-// TMEM (512 columns): Q (DH/2 columns of packed bf16) at 0, S buffers at 128 and 192 (64 fp32
-// columns each), O (DH columns) at 256; DH = head_dim / CL.
-//
-// CL = 2 (head_dim 512): a 128 x 512 fp32 O alone would fill the 512 TMEM columns of an SM,
-// so a cluster of two CTAs splits head_dim: CTA h holds Q[:, 256h:256h+256] and reads only
-// that half of K and V. Each computes a partial S over its half, sends it to its peer through
-// distributed shared memory, and adds the peer's partial to its own; each then accumulates and
-// writes its own half of O with its own P, m and l. No multiply-add is done twice. With k_eq_v
-// the K half is also the V half. The partial scores travel as fp16 (saturating) with
-// asynchronous stores into the peer's shared memory (st.async, completion counted in bytes on
-// the peer's mbarrier); each CTA keeps its own partial in fp32, so the peer's rounding moves a
-// score by at most 2^-11 of its partial.
+// TMEM (512 columns): Q (D/2 columns of packed bf16) at 0, S buffers at 128 and 192 (64 fp32
+// columns each), O (D columns) at 256.
 //
 // The key range of a unit is clamped to [first row's window start, last row's position] before
 // any load; rows of a K/V tile outside the range are zeroed in shared memory before they enter
@@ -65,19 +58,18 @@ constexpr int kFaKeys = 64;                   // keys per tile (N of S = Q K^T)
 constexpr int kFaSmemLimit = 232448;          // max dynamic shared memory per block
 constexpr float kLazyRescaleLog2 = 8.f;
 
-template <int D, int CL>
+template <int D>
 struct FaLayout {
-    static constexpr int DH = D / CL;                    // head_dim columns owned by a CTA
+    static constexpr int DH = D;                         // head_dim
     static constexpr int CHUNKS = DH / 64;               // 64-column boxes per K/V tile
     static constexpr int BOX = kFaKeys * 128;            // one box: 64 keys x 64 columns
     static constexpr int SLOT = CHUNKS * BOX;            // one K or V tile
     static constexpr int P_TILE = 128 * kFaKeys * 2;     // 128 rows x 64 keys bf16
-    static constexpr int X_TILE = CL > 1 ? 128 * kFaKeys * 2 : 0;  // peer's partial S (fp16)
     static constexpr int Q_COL = 0;                      // TMEM columns
     static constexpr int S_COL = 128;                    // + 64 * buffer
     static constexpr int O_COL = 256;
-    // fixed shared memory besides the ring: P (2), X (2), reference row maxima, barriers
-    static constexpr int FIXED = 2 * P_TILE + 2 * X_TILE + 512 + 512;
+    // fixed shared memory besides the ring: P (2), reference row maxima, barriers
+    static constexpr int FIXED = 2 * P_TILE + 512 + 512;
     static_assert(DH / 2 <= 128 && O_COL + DH <= 512, "TMEM budget");
     static_assert(2 * 128 * 8 <= P_TILE, "the epilogue's (m, l) exchange fits in one P buffer");
 };
@@ -88,7 +80,7 @@ struct FaParams {
     int batch;
     int n_rt;      // row tiles per (sequence, KV head)
     int n_units;   // n_rt * batch * n_kv
-    int n_workers; // CTAs (clusters) walking the units
+    int n_workers; // CTAs walking the units
 };
 
 // Non-blocking check of a phase's completion (cheaper than try_wait when it has completed).
@@ -214,13 +206,13 @@ struct FaTileIter {
 
 // SOFTCAP: the soft-capped variant (a separate instantiation, so that the plain kernel carries
 // no code for it)
-template <int D, int CL, bool SOFTCAP>
+template <int D, bool SOFTCAP>
 __global__ void __launch_bounds__(kFaThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const FaParams fp) {
     pdl_launch_dependents();
     pdl_wait();  // the previous kernel on the stream has completed
-    using Lay = FaLayout<D, CL>;
+    using Lay = FaLayout<D>;
     constexpr int DH = Lay::DH;
     const RowsParams& p = fp.p;
     extern __shared__ uint8_t smem_raw[];
@@ -229,8 +221,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     const int NS = fp.n_slots;
     uint8_t* slots = smem;
     uint8_t* sP = smem + NS * Lay::SLOT;                     // P buffers [2][128 x 64] bf16
-    uint8_t* sX = sP + 2 * Lay::P_TILE;                      // peer partials [2][8][128] x 16 B
-    float* mref = reinterpret_cast<float*>(sX + 2 * Lay::X_TILE);  // [128] softmax references
+    float* mref = reinterpret_cast<float*>(sP + 2 * Lay::P_TILE);  // [128] softmax references
     uint64_t* bars = reinterpret_cast<uint64_t*>(mref + 128);
     // Step i of the MMA warp issues S(i) and P V(i-2). step_ready[i % R] completes when the
     // step's K/V tiles have landed (producer arrival + transaction bytes) and P(i-2) is in
@@ -239,16 +230,13 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     // TMEM, P V(i-2) has completed (so P buffer i % 2 and the step's ring slots are free).
     uint64_t* step_ready = bars;
     uint64_t* step_done = bars + kFaSteps;
-    uint64_t* x_full = bars + 2 * kFaSteps;     // [2] the peer's partial S for group w landed
-    uint64_t* x_free = x_full + 2;              // [2] the peer has read what this CTA sent it
-    uint64_t* o_full = x_full + 4;              // a unit's last P V has completed
-    uint64_t* o_free = x_full + 5;              // the epilogue has read O
-    uint64_t* q_ready = x_full + 6;             // a unit's Q is in TMEM
-    uint64_t* m_ready = x_full + 7;             // the reference after tile T is in mref
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(x_full + 8);
+    uint64_t* o_full = bars + 2 * kFaSteps;     // a unit's last P V has completed
+    uint64_t* o_free = o_full + 1;              // the epilogue has read O
+    uint64_t* q_ready = o_full + 2;             // a unit's Q is in TMEM
+    uint64_t* m_ready = o_full + 3;             // the reference after tile T is in mref
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(o_full + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t h = CL > 1 ? cluster_rank() : 0u;  // which head_dim part this CTA owns
-    const int worker = blockIdx.x / CL;
+    const int worker = blockIdx.x;
 
     if (warp == kFaMmaWarp) {
         tmem_alloc(tslot, 512);
@@ -259,10 +247,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             mbar_init(&step_ready[i], 5);
             mbar_init(&step_done[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&x_full[i], 1);  // one local arrival with the exchange's byte count
-            mbar_init(&x_free[i], 4);  // the peer's four warps have read their copy
-        }
         mbar_init(o_full, 1);
         mbar_init(o_free, 8);
         mbar_init(q_ready, 4);
@@ -271,7 +255,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync();  // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tQ = tmem + Lay::Q_COL, tO = tmem + Lay::O_COL;
@@ -304,7 +287,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                 }
 #pragma unroll
                 for (int c = 0; c < Lay::CHUNKS; ++c)
-                    tma_load_3d(dst + c * Lay::BOX, map, (int)h * DH + c * 64, slot0, row3, bar);
+                    tma_load_3d(dst + c * Lay::BOX, map, c * 64, slot0, row3, bar);
             };
             FaTileIter it;
             it.init(fp, worker);
@@ -458,12 +441,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         const int r = threadIdx.x & 127;       // tile row = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         uint8_t* sPw = sP + w * Lay::P_TILE;
-        uint32_t peer_x = 0, peer_x_full = 0, peer_x_free = 0;
-        if (CL > 1) {
-            peer_x = map_to_peer(sX + w * Lay::X_TILE + 16 * r, h ^ 1u);
-            peer_x_full = map_to_peer(&x_full[w], h ^ 1u);
-            peer_x_free = map_to_peer(&x_free[w], h ^ 1u);
-        }
         bool ok = true;
 
         // this group's half of the output columns of a unit's rows
@@ -472,7 +449,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             const int tk = R / p.G, hd = U.kvh * p.G + (R - tk * p.G);
             return reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
                                             (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D +
-                                            h * DH + w * (DH / 2));
+                                            w * (DH / 2));
         };
         auto zero_unit = [&](const FaUnit& U) {  // a unit without tiles: zeros
             if (r < U.n_rows) {
@@ -480,7 +457,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 #pragma unroll 4
                 for (int j = 0; j < DH / 16; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
             }
-            if (U.bad && w == 0 && r == 0 && U.kvh == 0 && U.rt == 0 && h == 0)
+            if (U.bad && w == 0 && r == 0 && U.kvh == 0 && U.rt == 0)
                 report(p.err, U.bad_real ? GEMMA_DEVERR_N_REAL : GEMMA_DEVERR_SEQ_LEN);
         };
         // the unit's Q rows (this CTA's head_dim part) into TMEM, once S(T_prev) (the last S
@@ -495,7 +472,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             const int tk = R / p.G, hd = U.kvh * p.G + (R - tk * p.G);
             const uint4* qrow = reinterpret_cast<const uint4*>(
                 reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D + h * DH);
+                (((size_t)U.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D);
 #pragma unroll
             for (int hf = 0; hf < NQ / HALF; ++hf) {
                 uint4 qv[HALF];
@@ -559,7 +536,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                             const int tk = R / p.G, hd = U2.kvh * p.G + (R - tk * p.G);
                             const char* qrow = reinterpret_cast<const char*>(
                                 reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                (((size_t)U2.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D + h * DH);
+                                (((size_t)U2.b * p.n_tok + tk) * p.n_q + hd) * (size_t)D);
 #pragma unroll
                             for (int j = 0; j < (DH * 2) / 128; ++j)
                                 asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + j * 128));
@@ -586,41 +563,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                             s[e] = __uint_as_float(v0[e]);
                             s[32 + e] = __uint_as_float(v1[e]);
                         }
-                    }
-
-                    if (CL > 1) {
-                        // send this row's partial scores to the peer (asynchronous stores that
-                        // count bytes on the peer's x_full), then add the peer's partial
-                        const int k = T >> 1;
-                        if (r == 0) mbar_arrive_expect_tx(&x_full[w], 128 * kFaKeys * 2);
-                        if (k >= 1 && ok) ok = mbar_wait_cluster(&x_free[w], (k - 1) & 1, p.err);
-                        // chunk-major layout X[c][r] (16-byte chunks of 8 fp16 scores): a
-                        // warp's 32 stores of chunk c are one contiguous 512-byte write
-#pragma unroll
-                        for (int c = 0; c < kFaKeys / 8; ++c)
-                            st_async_v4(peer_x + c * (128 * 16), pack_f16_sat(s[8 * c], s[8 * c + 1]),
-                                        pack_f16_sat(s[8 * c + 2], s[8 * c + 3]),
-                                        pack_f16_sat(s[8 * c + 4], s[8 * c + 5]),
-                                        pack_f16_sat(s[8 * c + 6], s[8 * c + 7]), peer_x_full);
-                        if (ok) ok = mbar_wait_cluster(&x_full[w], k & 1, p.err);
-                        const uint4* xr = reinterpret_cast<const uint4*>(sX + w * Lay::X_TILE) + r;
-#pragma unroll
-                        for (int c = 0; c < kFaKeys / 8; ++c) {
-                            const uint4 x = xr[c * 128];
-                            const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 f = unpack_f16(wd[i]);
-                                const float2 t = f32x2_split(add_f32x2(
-                                    f32x2(s[8 * c + 2 * i], s[8 * c + 2 * i + 1]), f32x2(f.x, f.y)));
-                                s[8 * c + 2 * i] = t.x;
-                                s[8 * c + 2 * i + 1] = t.y;
-                            }
-                        }
-                        // every lane has consumed its loads of X[w] (the adds above): the peer may
-                        // overwrite it
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_remote_relaxed(peer_x_free);
                     }
 
                     // scores stay raw; scale > 0, so max(raw) * scale_log2 is the max of the
@@ -769,8 +711,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                             uint32_t v[32];
                             tmem_ld32(tO + lane_off + w * (DH / 2) + sl * SW + j * 32, v);
                             tmem_ld_wait();
-#pragma unroll
                             const unsigned long long inv2 = f32x2(inv, inv);
+#pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int c = j * 4 + e;
                                 uint32_t w4[4];
@@ -810,7 +752,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync();  // the peer no longer writes into this CTA's shared memory
     if (warp == kFaMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -818,9 +759,9 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int D, int CL>
+template <int D>
 static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
-    using Lay = FaLayout<D, CL>;
+    using Lay = FaLayout<D>;
     CUtensorMap km, vm;
     // [rows][slots][D]: rows = sequences x KV heads (pages x KV heads for a paged pool)
     const uint64_t map_slots = p.page_size ? (uint64_t)p.page_size : (uint64_t)p.cap;
@@ -836,44 +777,31 @@ static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
     if (ns < 3) return cudaErrorInvalidValue;
     const size_t smem = (size_t)ns * Lay::SLOT + fixed;
 
-    // per device: the shared-memory attribute, and how many CTAs (clusters) fit at once
+    // per device: the shared-memory attribute, and how many CTAs fit at once
     static std::atomic<int> workers[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     int n_workers = dev >= 0 && dev < 64 ? workers[dev].load(std::memory_order_relaxed) : 0;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kFaThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     if (n_workers <= 0) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL, false>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kFaSmemLimit);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D, CL, true>,
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kFaSmemLimit);
         if (e != cudaSuccess) return e;
         int n_sm = 0;
         e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        n_workers = n_sm / CL;
-        if (CL > 1) {
-            cudaLaunchConfig_t occ = cfg;
-            occ.gridDim = dim3(CL * n_workers);
-            int clusters = 0;
-            e = cudaOccupancyMaxActiveClusters(&clusters, prefill_tc_kernel<D, CL, false>, &occ);
-            if (e != cudaSuccess) return e;
-            if (clusters < 1) return cudaErrorInvalidConfiguration;
-            if (clusters < n_workers) n_workers = clusters;
-        }
+        n_workers = n_sm;
         if (dev >= 0 && dev < 64) workers[dev].store(n_workers, std::memory_order_relaxed);
     }
     FaParams fp;
@@ -883,9 +811,9 @@ static cudaError_t launch_d(const RowsParams& p, int batch, cudaStream_t st) {
     fp.n_rt = (p.n_tok * p.G + 127) / 128;
     fp.n_units = fp.n_rt * batch * p.n_kv;
     fp.n_workers = fp.n_units < n_workers ? fp.n_units : n_workers;
-    cfg.gridDim = dim3(CL * fp.n_workers);
-    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, true>, km, vm, fp)
-                           : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, CL, false>, km, vm, fp);
+    cfg.gridDim = dim3(fp.n_workers);
+    return p.softcap > 0.f ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, true>, km, vm, fp)
+                           : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, false>, km, vm, fp);
 }
 
 bool prefill_tc_supported(int head_dim) {
@@ -894,8 +822,8 @@ bool prefill_tc_supported(int head_dim) {
 
 cudaError_t launch_prefill_tc(const RowsParams& p, int head_dim, int batch, cudaStream_t st) {
     switch (head_dim) {
-        case 64: return launch_d<64, 1>(p, batch, st);
-        case 128: return launch_d<128, 1>(p, batch, st);
+        case 64: return launch_d<64>(p, batch, st);
+        case 128: return launch_d<128>(p, batch, st);
         case 256: return launch_prefill_pair(p, 256, batch, st);  // every supported group divides 128
         case 512: return launch_prefill_pair(p, 512, batch, st);
     }
