@@ -106,6 +106,9 @@ PREFILL_SHAPES = [
     # walks several units (each a few 128-key tiles); every output compared
     (LayerSpec(SLIDING, 256, 4, 2, 256, False), 768, [868, 800, 900, 768, 1000, 850, 790, 880],
      1024, None),
+    # head_dim 512 runs on clusters of two pairs: 40 units, more than there are clusters
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 64, [164, 67, 314, 128, 64, 244, 97, 264, 192, 141],
+     320, None),
 ]
 
 

@@ -32,7 +32,7 @@ CASES = [
     (LayerSpec(SLIDING, 1024, 16, 8, 256, False), 1, [4000, 1500], 4032),
     (LayerSpec(GLOBAL, 0, 8, 2, 128, False), 1, [5, 300], 320),
     (LayerSpec(SLIDING, 1024, 16, 8, 256, False), 128, [1300, 300], 1344),  # prefill, tcgen05
-    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 96, [700, 200], 704),         # 2-CTA cluster
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 96, [700, 200], 704),         # two CTA pairs
     (LayerSpec(SLIDING, 37, 8, 1, 64, False), 40, [100, 45], 128),
 ]
 
