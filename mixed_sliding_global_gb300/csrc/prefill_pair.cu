@@ -1,12 +1,12 @@
-// prefill_pair.cu -- prefill-bucket attention at head_dim 256 on CTA pairs (the 2-SM form of the
-// 5th-generation tensor-core MMA, tcgen05 with cta_group::2).
+// prefill_pair.cu -- prefill-bucket attention at head_dim 256 and 512 on CTA pairs (the 2-SM form
+// of the 5th-generation tensor-core MMA, tcgen05 with cta_group::2).
 //
 // Computes, for tiles of 256 query rows (rows = (token, head of the GQA group) pairs, token
 // major, so every row of a tile reads the same KV head), softmax(scale * Q K^T) V over the
 // causal (and, on sliding layers, windowed) key range of each row, with the K/V cache of the
 // owner layer ("Porting Gemma-4 (2B / 4B / 12B) to AWS Inferentia2", sections 2.1-2.3; the
 // pages' "eager" matmul-softmax-matmul definition, section 4.3). The sliding layers of every
-// Gemma-4 size have head_dim 256.
+// Gemma-4 size have head_dim 256, the global layers 512.
 //
 // A cluster of two CTAs (one per SM) runs each MMA as one instruction of M = 256: CTA c owns
 // rows 128c..128c+127 of the tile (its Q rows in its shared memory, its rows of S, P and O in
@@ -16,6 +16,14 @@
 // So a 128-key step needs 64 KB of shared memory per SM (a one-SM 128-key step needs 128 KB),
 // S runs at N = 128 (an MMA of N = 64 costs as much as one of N = 128), and one step issues 24
 // MMAs where one-SM 64-key steps issue 40 for the same keys.
+//
+// Head_dim 512 (H = 2): a 128-row O of 512 fp32 columns alone would fill one SM's tensor memory,
+// so a cluster holds two pairs, pair h owning columns 256h..256h+255 of Q, K, V and O and running
+// everything above on them. Its S is a partial over its half: each softmax group sends its
+// columns of the partial to the partner CTA (cluster rank ^ 2) as saturating fp16 with st.async
+// (bytes counted on the partner's mbarrier), and adds the partner's partial to its own fp32 one,
+// so the partner's rounding moves a score by at most 2^-11 of its partial. The ring has 3 slots
+// to make room for the 32 KB receive buffer.
 //
 // Persistent grid: each pair walks work units = (256-row tile, sequence, KV head), latest row
 // tiles (longest key ranges) first; the 128-key tiles of all its units form one flat sequence.
@@ -41,7 +49,8 @@
 // rows) orders those writes before the async proxy with a proxy fence first, and one that read
 // or wrote tensor memory fences its tcgen05 operations before the arrival.
 // TMEM (512 columns per CTA): S (128 fp32) at 0, P (2 x 64 columns of packed bf16) at 128, O
-// (256 fp32) at 256. Shared memory: the ring (4 slots), Q (64 KB), the epilogue's staging.
+// (256 fp32) at 256. Shared memory: the ring (4 slots; 3 at head_dim 512), Q (64 KB), the
+// epilogue's staging (O / l leaves in 32-column slices by TMA tensor stores).
 // The Q rows of a 128-row half tile are G consecutive heads of 128 / G consecutive tokens, one
 // TMA box per 64 columns; the kernel needs G to divide 128.
 //
