@@ -106,6 +106,10 @@ PREFILL_SHAPES = [
     # walks several units (each a few 128-key tiles); every output compared
     (LayerSpec(SLIDING, 256, 4, 2, 256, False), 768, [868, 800, 900, 768, 1000, 850, 790, 880],
      1024, None),
+    # groups of 4 and 8 query heads on the pair kernels (Q and output boxes of G heads x 128 / G
+    # tokens)
+    (LayerSpec(SLIDING, 100, 16, 4, 256, False), 70, [200, 90], 256, None),
+    (LayerSpec(GLOBAL, 0, 8, 1, 512, True), 50, [120, 50], 128, None),
     # head_dim 512 runs on clusters of two pairs: 40 units, more than there are clusters
     (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 64, [164, 67, 314, 128, 64, 244, 97, 264, 192, 141],
      320, None),
