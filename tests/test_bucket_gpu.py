@@ -128,3 +128,25 @@ def test_bad_n_real_is_reported_and_zeroed():
     assert err.item() & g.GEMMA_DEVERR_N_REAL
     assert out[0].abs().sum().item() == 0
     assert out[1, :10].abs().sum().item() > 0 and out[1, 10:].abs().sum().item() == 0
+
+
+@pytest.mark.parametrize("d,kind,n_q,n_kv,keqv", [(256, SLIDING, 16, 8, False),
+                                                  (512, GLOBAL, 16, 1, True)])
+def test_prefill_bad_seq_len_is_reported_and_zeroed(d, kind, n_q, n_kv, keqv):
+    """A sequence whose length is below its new tokens: reported, its rows zeros; the other
+    sequence is unaffected (both CTA-pair kernels)."""
+    B, n_new, cap = 2, 40, 256
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    q = torch.randn(B, n_new, n_q, d, device="cuda", generator=gen).bfloat16()
+    kc = torch.randn(B, n_kv, cap, d, device="cuda", generator=gen).bfloat16()
+    vc = None if keqv else torch.randn(B, n_kv, cap, d, device="cuda", generator=gen).bfloat16()
+    lens = torch.tensor([100, 20], dtype=torch.int32, device="cuda")   # 20 < n_new
+    out = torch.full_like(q, 7.0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g.gemma_attn_prefill(out, q, [kc], [vc], [0], 0, lens, 100, kind=kind,
+                         window=64 if kind == SLIDING else 0, n_kv=n_kv, k_eq_v=keqv,
+                         scale=d ** -0.5, device_error=err)
+    torch.cuda.synchronize()
+    assert err.item() & g.GEMMA_DEVERR_SEQ_LEN
+    assert out[1].float().abs().sum().item() == 0
+    assert torch.isfinite(out[0].float()).all() and out[0].float().abs().sum().item() > 0
