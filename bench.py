@@ -50,6 +50,11 @@ PAGE_EXAMPLE = 256      # keys per page of the paged pools
 # recorded value
 NCU_DECODE_TRAFFIC = {"source_sha1": "1c8bdee02750be5f2e34501c5f8a00e979df57e3",
                       "per_algorithmic_byte": {"sliding": 1.0154, "global": 1.0344}}
+# dram bytes (read + write) per launch of the prefill pair kernels on the default prefill
+# workload (batch 4, 512 tokens onto 3584), from one ncu capture of a sliding and a global
+# layer; used only for that workload and while the kernel sources hash to the recorded value
+NCU_PREFILL_TRAFFIC = {"source_sha1": None, "batch": 4, "n_new": 512, "ctx": 4096,
+                       "bytes_per_launch": {"sliding": None, "global": None}}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -100,9 +105,12 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha1():
+PREFILL_SOURCES = ("prefill_pair.cu", "tc.cuh", "common.cuh", "attn_internal.h")
+
+
+def kernel_source_sha1(names=("rows_attn.cu", "common.cuh", "attn_internal.h")):
     h = hashlib.sha1()
-    for name in ("rows_attn.cu", "common.cuh", "attn_internal.h"):
+    for name in names:
         with open(os.path.join(ROOT, "mixed_sliding_global_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -909,12 +917,24 @@ def run_native(args):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": None,
                 "kernel": "attention launch (prefill)", "peak_source": peak_src + " sustained"}
+        tr = NCU_PREFILL_TRAFFIC
+        traffic_ok = (tr["source_sha1"] is not None and
+                      tr["source_sha1"] == kernel_source_sha1(PREFILL_SOURCES) and
+                      args.softcap is None and
+                      (w.batch, w.n_new, max(w.ctx_lens)) == (tr["batch"], tr["n_new"], tr["ctx"]))
+        n_launch, traffic_sum = 0, 0.0
         for kind, name in ((synth.SLIDING, "sliding"), (synth.GLOBAL, "global")):
             ls = [l for l, s in enumerate(w.layers) if s.kind == kind]
             if ls:
                 f = sum(per_flops[l] for l in ls)
                 t = sum(launch_ms[l] for l in ls)
-                roof[name] = {"tflops": f / (t * 1e-3) / 1e12, "launch_us": 1e3 * t / len(ls)}
+                roof[name] = {"tflops": f / (t * 1e-3) / 1e12, "launch_us": 1e3 * t / len(ls),
+                              "traffic": tr["bytes_per_launch"][name] if traffic_ok else None}
+                if traffic_ok:
+                    n_launch += len(ls)
+                    traffic_sum += len(ls) * tr["bytes_per_launch"][name]
+        # per attention launch of the step, averaged over its launches
+        roof["traffic"] = traffic_sum / n_launch if n_launch else None
 
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
