@@ -89,7 +89,7 @@ class DeviceRun:
                                d["write_pos"], k_eq_v=spec.k_eq_v, device_error=self.err)
 
     def attend(self, l: int, max_seq_len: Optional[int] = None,
-               softcap: Optional[float] = None) -> torch.Tensor:
+               softcap: Optional[float] = None, prefill_entry: bool = False) -> torch.Tensor:
         w, spec, d = self.w, self.w.layers[l], self.dev[l]
         msl = max(w.ctx_lens) if max_seq_len is None else max_seq_len
         q = d["q"]
@@ -104,7 +104,9 @@ class DeviceRun:
             self.g.gemma_attn_softcap(out, q, self.kc, self.vc, w.owner_map, l, d["seq_lens"], msl,
                                       softcap=softcap, **kw)
         else:
-            fn = self.g.gemma_attn_decode if w.n_new == 1 else self.g.gemma_attn_prefill
+            # prefill_entry: one new token through gemma_attn_prefill instead of the decode entry
+            fn = self.g.gemma_attn_decode if w.n_new == 1 and not prefill_entry \
+                else self.g.gemma_attn_prefill
             fn(out, q, self.kc, self.vc, w.owner_map, l, d["seq_lens"], msl, **kw)
         return out
 

@@ -15,7 +15,7 @@ from harness import DeviceRun, compare, host_inputs, oracle_outputs
 pytestmark = pytest.mark.gpu
 
 
-def run_and_compare(w, layers, seqs=None, q_range=None, max_seq_len=None):
+def run_and_compare(w, layers, seqs=None, q_range=None, max_seq_len=None, prefill_entry=False):
     hb = host_inputs(w, layers, seqs)
     ref = oracle_outputs(w, hb, layers, q_range)
     gr = DeviceRun(w, hb)
@@ -23,7 +23,7 @@ def run_and_compare(w, layers, seqs=None, q_range=None, max_seq_len=None):
     for l in layers:
         if w.is_owner(l):
             gr.append(l)
-        got[l] = gr.attend(l, max_seq_len)
+        got[l] = gr.attend(l, max_seq_len, prefill_entry=prefill_entry)
     torch.cuda.synchronize()
     assert gr.err.item() == 0, f"device error word {gr.err.item()}"
     errs = {}
@@ -113,6 +113,11 @@ PREFILL_SHAPES = [
     # head_dim 512 runs on clusters of two pairs: 40 units, more than there are clusters
     (LayerSpec(GLOBAL, 0, 16, 1, 512, True), 64, [164, 67, 314, 128, 64, 244, 97, 264, 192, 141],
      320, None),
+    # a window of one key on the pair kernels: every query attends only itself (the output is
+    # its own V row), so most of each 128-key tile is masked for every row, and at head_dim 512
+    # the partners swap partial scores that are mostly masked
+    (LayerSpec(SLIDING, 1, 4, 2, 256, False), 40, [40, 300], 320, None),
+    (LayerSpec(SLIDING, 1, 4, 1, 512, True), 20, [20, 150], 160, None),
 ]
 
 
@@ -120,6 +125,15 @@ PREFILL_SHAPES = [
 def test_prefill_shapes(case):
     spec, n_new, lens, cap, qr = PREFILL_SHAPES[case]
     run_and_compare(one_layer(spec, n_new, lens, cap), [0], q_range=qr)
+
+
+# One new token through the prefill entry (at these head_dims the tensor-core pair kernels: one
+# or two real rows of a 256-row unit), with a sequence of length 1 whose token attends only
+# itself; the result must be the decode's.
+@pytest.mark.parametrize("spec", [LayerSpec(GLOBAL, 0, 2, 1, 256, False),
+                                  LayerSpec(SLIDING, 3, 16, 1, 512, True)])
+def test_prefill_entry_with_one_new_token(spec):
+    run_and_compare(one_layer(spec, 1, [1, 77, 130], 160), [0], prefill_entry=True)
 
 
 @pytest.mark.parametrize("case", [0, 1, 3])
