@@ -127,9 +127,8 @@ def test_prefill_shapes(case):
     run_and_compare(one_layer(spec, n_new, lens, cap), [0], q_range=qr)
 
 
-# One new token through the prefill entry (at these head_dims the tensor-core pair kernels: one
-# or two real rows of a 256-row unit), with a sequence of length 1 whose token attends only
-# itself; the result must be the decode's.
+# One new token through the prefill entry (served by the decode kernels, split over key chunks
+# with the workspace), with a sequence of length 1 whose token attends only itself.
 @pytest.mark.parametrize("spec", [LayerSpec(GLOBAL, 0, 2, 1, 256, False),
                                   LayerSpec(SLIDING, 3, 16, 1, 512, True)])
 def test_prefill_entry_with_one_new_token(spec):
