@@ -106,10 +106,12 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-PREFILL_SOURCES = ("prefill_pair.cu", "tc.cuh", "common.cuh", "attn_internal.h")
+# the sources (and every header they include) of the kernels whose ncu traffic is recorded
+DECODE_SOURCES = ("rows_attn.cu", "common.cuh", "tc.cuh", "tmap.h", "attn_internal.h")
+PREFILL_SOURCES = ("prefill_pair.cu", "common.cuh", "tc.cuh", "tmap.h", "attn_internal.h")
 
 
-def kernel_source_sha1(names=("rows_attn.cu", "common.cuh", "attn_internal.h")):
+def kernel_source_sha1(names=DECODE_SOURCES):
     h = hashlib.sha1()
     for name in names:
         with open(os.path.join(ROOT, "mixed_sliding_global_gb300", "csrc", name), "rb") as f:

@@ -111,6 +111,12 @@ GEMMA_DEVINL float fast_rcp(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// tanh(x) (the SFU's approximation: relative error about 2^-11, one instruction)
+GEMMA_DEVINL float fast_tanh(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // ---------------------------------------------------------------------------------------------
 // MMA descriptors
