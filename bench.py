@@ -48,14 +48,14 @@ PAGE_EXAMPLE = 256      # keys per page of the paged pools
 # of each launch kind (a batch-40 sliding layer in the unsplit launch configuration of the
 # batch-64 one, and a batch-64 global layer); used only while the kernel sources hash to the
 # recorded value
-NCU_DECODE_TRAFFIC = {"source_sha1": "a9d2d11bf3491644f61a62b41c93ced99ad34d22",
-                      "per_algorithmic_byte": {"sliding": 1.0144, "global": 1.0347}}
+NCU_DECODE_TRAFFIC = {"source_sha1": "6045a0b6c038e3b758a6b23a20925842b6f34c5c",
+                      "per_algorithmic_byte": {"sliding": 1.0153, "global": 1.0349}}
 # dram bytes (read + write) per launch of the prefill pair kernels on the default prefill
 # workload (batch 4, 512 tokens onto 3584), from one ncu capture of a sliding and a global
 # layer; used only for that workload and while the kernel sources hash to the recorded value
-NCU_PREFILL_TRAFFIC = {"source_sha1": "e6d73310d4ac82368cdaafad0f15d242a976ce0a", "batch": 4, "n_new": 512,
-                       "ctx": 4096, "bytes_per_launch": {"sliding": 73982208 + 2482432,
-                                                         "global": 50624768 + 547584}}
+NCU_PREFILL_TRAFFIC = {"source_sha1": "7a60a956b29b85548b4ee17df470bd4815000449", "batch": 4, "n_new": 512,
+                       "ctx": 4096, "bytes_per_launch": {"sliding": 74000128 + 2386688,
+                                                         "global": 50580480 + 519424}}
 
 
 # ---------------------------------------------------------------------------------------------
