@@ -38,10 +38,11 @@ def expected_ring(lin_appended, lens, R):
     return ring
 
 
-def run_ring(w, R, fused=False, ring_in=None):
+def run_ring(w, R, fused=False, ring_in=None, softcap=None, q_gain=1.0):
     spec = w.layers[0]
     hb = host_inputs(w, [0])
     b0 = hb[0]
+    b0.q.mul_(q_gain)  # (a power of two: exact in bf16)
     dev = "cuda"
     kr = to_ring(b0.k_cache, b0.write_pos, R).to(dev)
     vr = to_ring(b0.v_cache, b0.write_pos, R).to(dev) if b0.v_cache is not None else None
@@ -62,8 +63,11 @@ def run_ring(w, R, fused=False, ring_in=None):
     else:
         g.gemma_kv_append_ring([kr], [vr], [0], 0, kn, vn, wp, k_eq_v=spec.k_eq_v,
                                device_error=err)
-        fn = g.gemma_attn_decode if w.n_new == 1 else g.gemma_attn_prefill
-        fn(out, q, [kr], [vr], [0], 0, lens, msl, **kw)
+        if softcap is not None:
+            g.gemma_attn_softcap(out, q, [kr], [vr], [0], 0, lens, msl, softcap=softcap, **kw)
+        else:
+            fn = g.gemma_attn_decode if w.n_new == 1 else g.gemma_attn_prefill
+            fn(out, q, [kr], [vr], [0], 0, lens, msl, **kw)
     torch.cuda.synchronize()
     assert err.item() == 0
     return hb, out, kr, vr
@@ -97,6 +101,16 @@ def test_ring_matches_oracle(spec, n_new, ctx, R, dtype):
     lens = [int(x) for x in b0.seq_lens]
     assert torch.equal(kr.cpu(), expected_ring(lin, lens, R))
     assert torch.equal(vr.cpu(), expected_ring(linv, lens, R))
+
+
+# the soft-capped entry point on ring caches: decode (split keys), the CTA-pair prefill, and the
+# one-SM prefill at head_dim 64; queries scaled so that the cap bites
+@pytest.mark.parametrize("case", [0, 4, 5])
+def test_ring_softcap_matches_oracle(case):
+    spec, n_new, ctx, R = CASES[case]
+    w = one_layer(spec, n_new, ctx, BF16)
+    hb, out, _, _ = run_ring(w, R, softcap=30.0, q_gain=2.0)
+    compare(out, oracle_outputs(w, hb, [0], softcap=30.0)[0], BF16)
 
 
 def test_ring_fused_decode_equals_append_then_decode():
