@@ -342,7 +342,10 @@ int gemma_logit_softcap_argmax(const void* logits, int batch, int vocab, gemma_d
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of scratch gemma_logit_softcap_argmax needs on the current device ((size_t)-1 for
- * batch < 0 or vocab < 1). */
+ * batch < 0 or vocab < 1). 0 when the batch is large enough for every row to get CTAs of its
+ * own (at most 16, one thread-block cluster per row, reducing the row's index among themselves
+ * in the same launch); otherwise the rows' pieces meet in the scratch and a second launch
+ * reduces them. */
 size_t gemma_logit_workspace_size(int batch, int vocab);
 
 /* A static, human-readable name of a gemma_status value. */

@@ -53,8 +53,20 @@ def test_shapes(orc, dtype, batch, vocab, softcap):
 
 
 def test_full_size_batch_64(orc):
-    """The greedy step of the pages' vocabulary at batch 64 (bf16, cap 30), every row."""
+    """The greedy step of the pages' vocabulary at batch 64 (bf16, cap 30), every row: each
+    row's CTAs reduce its index in one launch (a cluster per row, no workspace)."""
+    assert g.gemma_logit_workspace_size(64, synth.VOCAB) == 0
     check(orc, synth.logits(64, synth.VOCAB, seed=1), synth.LOGIT_SOFTCAP)
+
+
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.FP32])
+def test_one_long_row_two_launches(orc, dtype):
+    """A single row too long for one cluster of CTAs: the pieces meet in the workspace and a
+    second launch reduces them."""
+    assert g.gemma_logit_workspace_size(1, 1 << 23) > 0
+    x = synth.logits(1, 1 << 23, seed=11, dtype=dtype)
+    x[0, (1 << 23) - 5] = x[0].float().max().item() + 1.0  # the maximum late in the row
+    check(orc, x, 30.0)
 
 
 @pytest.mark.parametrize("dtype", [synth.BF16, synth.FP32])
