@@ -111,6 +111,18 @@ DECODE_SOURCES = ("rows_attn.cu", "common.cuh", "tc.cuh", "tmap.h", "attn_intern
 PREFILL_SOURCES = ("prefill_pair.cu", "common.cuh", "tc.cuh", "tmap.h", "attn_internal.h")
 
 
+def prefill_traffic(w, softcap=None, n_real=None):
+    """DRAM bytes per attention launch of each layer kind from the recorded ncu capture, or
+    None where it does not apply (another workload, the soft-capped or padded entry point, or
+    kernel sources that no longer hash to the captured version)."""
+    tr = NCU_PREFILL_TRAFFIC
+    if (tr["source_sha1"] is None or softcap is not None or n_real is not None or
+            tr["source_sha1"] != kernel_source_sha1(PREFILL_SOURCES) or
+            (w.batch, w.n_new, max(w.ctx_lens)) != (tr["batch"], tr["n_new"], tr["ctx"])):
+        return None
+    return tr["bytes_per_launch"]
+
+
 def kernel_source_sha1(names=DECODE_SOURCES):
     h = hashlib.sha1()
     for name in names:
@@ -920,11 +932,8 @@ def run_native(args):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": None,
                 "kernel": "attention launch (prefill)", "peak_source": peak_src + " sustained"}
-        tr = NCU_PREFILL_TRAFFIC
-        traffic_ok = (tr["source_sha1"] is not None and
-                      tr["source_sha1"] == kernel_source_sha1(PREFILL_SOURCES) and
-                      args.softcap is None and
-                      (w.batch, w.n_new, max(w.ctx_lens)) == (tr["batch"], tr["n_new"], tr["ctx"]))
+        tr = prefill_traffic(w, args.softcap)
+        traffic_ok = tr is not None
         n_launch, traffic_sum = 0, 0.0
         for kind, name in ((synth.SLIDING, "sliding"), (synth.GLOBAL, "global")):
             ls = [l for l, s in enumerate(w.layers) if s.kind == kind]
@@ -932,10 +941,10 @@ def run_native(args):
                 f = sum(per_flops[l] for l in ls)
                 t = sum(launch_ms[l] for l in ls)
                 roof[name] = {"tflops": f / (t * 1e-3) / 1e12, "launch_us": 1e3 * t / len(ls),
-                              "traffic": tr["bytes_per_launch"][name] if traffic_ok else None}
+                              "traffic": tr[name] if traffic_ok else None}
                 if traffic_ok:
                     n_launch += len(ls)
-                    traffic_sum += len(ls) * tr["bytes_per_launch"][name]
+                    traffic_sum += len(ls) * tr[name]
         # per attention launch of the step, averaged over its launches
         roof["traffic"] = traffic_sum / n_launch if n_launch else None
 
@@ -1019,12 +1028,20 @@ def run_native(args):
                                    "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                                    "frac": ach / peaks["bf16_tflops_sustained"],
                                    "peak_source": peak_src + " sustained"}
+                tr2 = prefill_traffic(w2, cap2, real2)
+                n2, tsum2 = 0, 0.0
                 for kind, nm in ((synth.SLIDING, "sliding"), (synth.GLOBAL, "global")):
                     ls = [l for l, s in enumerate(w2.layers) if s.kind == kind]
                     f = sum(prefill_flops(w2, l, real2) for l in ls)
                     t = sum(lm2[l] for l in ls)
                     ent["roofline"][nm] = {"tflops": f / (t * 1e-3) / 1e12,
-                                           "launch_us": 1e3 * t / len(ls)}
+                                           "launch_us": 1e3 * t / len(ls),
+                                           "traffic": tr2[nm] if tr2 else None}
+                    if tr2:
+                        n2 += len(ls)
+                        tsum2 += len(ls) * tr2[nm]
+                # DRAM bytes per attention launch, averaged over the step's launches
+                ent["roofline"]["traffic"] = tsum2 / n2 if n2 else None
             if rot > 1:
                 ent["l2"] = f"{rot} rotating input copies"
             if cap2 is not None:
