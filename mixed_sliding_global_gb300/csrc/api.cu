@@ -85,6 +85,10 @@ struct Plan {
 // the portable cluster size; fewer keys per CTA matter more there than the wider merge).
 constexpr int kMaxClusterSplit = 8;
 constexpr int kMaxBigClusterSplit = 16;
+// A latency-bound plan finer than the largest cluster is coarsened to one cluster of
+// kMaxBigClusterSplit chunks (no combine launch) while each chunk stays at most this many keys
+// (a few key tiles per CTA; longer chunks cost more per CTA than the combine pass saves).
+constexpr long long kBigClusterMaxKeys = 128;
 
 // Decode splits each (sequence, KV head) key range into chunks so that enough CTAs stream
 // the cache at once: about one chunk per SM for small problems, about eight per SM (and at
@@ -115,6 +119,15 @@ Plan make_plan(int batch, int kind, int window, int n_q, int n_kv, int head_dim,
     }
     if (n_split <= 1) return pl;
     if (n_split <= kMaxBigClusterSplit && (long long)batch * n_kv * n_split <= n_sm) {
+        pl.n_split = (int)n_split;
+        pl.chunk = (int)chunk;
+        pl.cluster = 1;
+        return pl;
+    }
+    if (n_split > kMaxBigClusterSplit && (long long)batch * n_kv * kMaxBigClusterSplit <= n_sm &&
+        n_read <= kMaxBigClusterSplit * kBigClusterMaxKeys) {
+        chunk = round_up((n_read + kMaxBigClusterSplit - 1) / kMaxBigClusterSplit, T);
+        n_split = (n_read + chunk - 1) / chunk;
         pl.n_split = (int)n_split;
         pl.chunk = (int)chunk;
         pl.cluster = 1;
