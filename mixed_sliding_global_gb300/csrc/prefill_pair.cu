@@ -80,6 +80,7 @@ constexpr int kPrQBytes = 128 * 256 * 2;      // a CTA's Q rows: 4 boxes of 128 
 constexpr int kPrQBox = 128 * 128;            // one of them
 constexpr int kPrStage = 2 * 128 * 64;        // epilogue: 2 groups x 128 rows x 32 columns bf16
 constexpr int kPrSmemLimit = 232448;          // max dynamic shared memory per block
+constexpr int kPrListMax = 512;               // units a padded bucket's work list holds
 constexpr float kPrLazyLog2 = 8.f;
 constexpr int kPrSCol = 0, kPrPCol = 128, kPrOCol = 256;  // TMEM columns
 // H parts of head_dim (256 columns each): a cluster of H pairs. Shared memory: ring, Q,
@@ -95,7 +96,8 @@ struct PrLay {
     static constexpr int X_BYTES = H == 2 ? 128 * kPrKeys * 2 : 0;
     static constexpr int MX_OFF = X_OFF + X_BYTES;
     static constexpr int BAR_OFF = MX_OFF + (2 * 2 * 128 + 2 * 128) * 4;
-    static constexpr int SMEM = BAR_OFF + 256 + 1024;  // + barriers, + alignment slack
+    static constexpr int ULIST_OFF = BAR_OFF + 256;    // a padded bucket's work list
+    static constexpr int SMEM = ULIST_OFF + (kPrListMax + 1) * 4 + 1024;  // + alignment slack
     static_assert(SMEM <= kPrSmemLimit, "shared memory budget");
 };
 
@@ -162,12 +164,18 @@ struct PrTile {
     int row0;      // the unit's first row
 };
 
+// LIST (a padded bucket): the units come from the work list in shared memory, entry j to
+// worker j mod W, the units with key tiles first (so that pad rows' empty units take no
+// worker's turn); otherwise worker w takes units w, w + W, w + 2W, ...
+template <bool LIST>
 struct PrTileIter {
     int u, stride, t, ord;
+    const int* list;
     PrUnit U;
-    __device__ __forceinline__ void init(const PrParams& fp, int worker) {
+    __device__ __forceinline__ void init(const PrParams& fp, int worker, const int* ulist) {
         u = worker - fp.n_pairs;  // next() advances to the first unit
         stride = fp.n_pairs;
+        list = ulist;
         t = 0;
         ord = -1;
         U.n_tiles = 0;
@@ -178,7 +186,7 @@ struct PrTileIter {
         while (t >= U.n_tiles) {
             u += stride;
             if (u >= fp.n_units) return T;
-            U = pr_unit(fp, u);
+            U = pr_unit(fp, LIST ? list[u] : u);
             t = 0;
             if (U.n_tiles > 0) ++ord;
         }
@@ -199,9 +207,9 @@ struct PrTileIter {
 
 }  // namespace
 
-// SOFTCAP: the soft-capped variant (a separate instantiation, so that the plain kernel carries
-// no code for it)
-template <int H, bool SOFTCAP>
+// SOFTCAP: the soft-capped variant; LIST: a padded bucket's, dealing out its units from the work
+// list (separate instantiations, so that the plain kernel carries no code for either)
+template <int H, bool SOFTCAP, bool LIST>
 __global__ void __launch_bounds__(kPrThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
@@ -271,6 +279,45 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             mbar_init(&x_free[i], 4);  // the partner's four warps of the group have read it
         }
         fence_barrier_init();
+    }
+    // a padded bucket's work list: every thread evaluates units, warp 0 lists those with key
+    // tiles first (in order), then the others
+    int* ulist = reinterpret_cast<int*>(smem + Lay::ULIST_OFF);
+    if constexpr (LIST) {
+        for (int u = threadIdx.x; u < fp.n_units; u += blockDim.x)
+            ulist[u] = pr_unit(fp, u).n_tiles > 0 ? 1 : 0;  // a flag first, then the entry
+        __syncthreads();
+        if (warp == 0) {
+            // lane l owns units [16 l, 16 l + 16): its count of units with tiles, and the lanes
+            // before it by a scan
+            constexpr int PER = kPrListMax / 32;
+            int flags = 0, cnt = 0;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int u = PER * lane + i;
+                const int f = u < fp.n_units ? ulist[u] : 0;
+                flags |= f << i;
+                cnt += f;
+            }
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int n_work = __shfl_sync(0xffffffffu, incl, 31);
+            __syncwarp();  // every lane has read its flags before any entry is written
+            int w_pos = incl - cnt;                            // next slot: a unit with tiles
+            int z_pos = n_work + PER * lane - (incl - cnt);    // and one without
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int u = PER * lane + i;
+                if (u < fp.n_units) {
+                    if ((flags >> i) & 1) ulist[w_pos++] = u;
+                    else ulist[z_pos++] = u;
+                }
+            }
+        }
     }
     __syncthreads();
     // every CTA of the cluster runs and its barriers exist before the pair allocation, any
@@ -350,8 +397,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     }
                 }
             };
-            PrTileIter it;
-            it.init(fp, worker);
+            PrTileIter<LIST> it;
+            it.init(fp, worker, ulist);
             PrTile prev;
             prev.valid = false;
             int Tn = 0;
@@ -406,8 +453,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             if (ok) ok = mbar_wait(&pfull[s], ph, p.err);
             return s;
         };
-        PrTileIter it;
-        it.init(fp, worker);
+        PrTileIter<LIST> it;
+        it.init(fp, worker, ulist);
         PrTile prev;
         prev.valid = false;
         int Tn = 0;  // index of `cur` in the flat tile sequence
@@ -484,8 +531,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             __syncwarp();
         };
         const uint32_t q_pfull0 = map_to_peer(q_pfull, lead);
-        PrTileIter it;
-        it.init(fp, worker);
+        PrTileIter<LIST> it;
+        it.init(fp, worker, ulist);
         PrTile prev;
         prev.valid = false;
         for (;;) {
@@ -547,7 +594,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             for (;;) {
                 u += fp.n_pairs;
                 if (u >= fp.n_units) return false;
-                U = pr_unit(fp, u);
+                U = pr_unit(fp, LIST ? ulist[u] : u);
                 if (U.n_tiles > 0) return true;
                 zero_unit(U);
             }
@@ -565,7 +612,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     hi = pos + 1;
                 }
                 // the next unit's Q rows towards L2 while this unit runs
-                if (cur.n_tiles > 2) {
+                if (!LIST && cur.n_tiles > 2) {
                     const int u2 = u + fp.n_pairs;
                     if (u2 < fp.n_units) {
                         const PrUnit U2 = pr_unit(fp, u2);
@@ -855,10 +902,13 @@ static cudaError_t launch_pair(const RowsParams& p, int batch, cudaStream_t st) 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (n_clusters <= 0) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<H, false>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<H, false, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_pair_kernel<H, true>,
+            e = cudaFuncSetAttribute(prefill_pair_kernel<H, true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_pair_kernel<H, false, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
         if (e != cudaSuccess) return e;
         int n_sm = 0;
@@ -868,7 +918,7 @@ static cudaError_t launch_pair(const RowsParams& p, int batch, cudaStream_t st) 
         cudaLaunchConfig_t occ = cfg;
         occ.gridDim = dim3(2 * H * n_clusters);
         int fit = 0;
-        e = cudaOccupancyMaxActiveClusters(&fit, prefill_pair_kernel<H, false>, &occ);
+        e = cudaOccupancyMaxActiveClusters(&fit, prefill_pair_kernel<H, false, false>, &occ);
         if (e != cudaSuccess) return e;
         if (fit < 1) return cudaErrorInvalidConfiguration;
         if (fit < n_clusters) n_clusters = fit;
@@ -881,9 +931,12 @@ static cudaError_t launch_pair(const RowsParams& p, int batch, cudaStream_t st) 
     fp.n_units = fp.n_rt * batch * p.n_kv;
     fp.n_pairs = fp.n_units < n_clusters ? fp.n_units : n_clusters;
     cfg.gridDim = dim3(2 * H * fp.n_pairs);
-    return p.softcap > 0.f
-               ? cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, true>, km, vm, qm, om, fp)
-               : cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, false>, km, vm, qm, om, fp);
+    if (p.softcap > 0.f)
+        return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, true, false>, km, vm, qm, om, fp);
+    // a padded bucket deals out its units with key tiles first (the work list)
+    if (p.n_real && fp.n_units <= kPrListMax)
+        return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, false, true>, km, vm, qm, om, fp);
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, false, false>, km, vm, qm, om, fp);
 }
 
 cudaError_t launch_prefill_pair(const RowsParams& p, int head_dim, int batch, cudaStream_t st) {
