@@ -933,8 +933,10 @@ static cudaError_t launch_pair(const RowsParams& p, int batch, cudaStream_t st) 
     cfg.gridDim = dim3(2 * H * fp.n_pairs);
     if (p.softcap > 0.f)
         return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, true, false>, km, vm, qm, om, fp);
-    // a padded bucket deals out its units with key tiles first (the work list)
-    if (p.n_real && fp.n_units <= kPrListMax)
+    // a padded bucket deals out its units with key tiles first (the work list) where the units
+    // of a row tile divide the workers evenly, so that the plain order would give a worker the
+    // same sequences in every wave (elsewhere building the list costs more than it saves)
+    if (p.n_real && fp.n_units <= kPrListMax && fp.n_pairs % (batch * p.n_kv) == 0)
         return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, false, true>, km, vm, qm, om, fp);
     return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<H, false, false>, km, vm, qm, om, fp);
 }
