@@ -53,9 +53,9 @@ NCU_DECODE_TRAFFIC = {"source_sha1": "6045a0b6c038e3b758a6b23a20925842b6f34c5c",
 # dram bytes (read + write) per launch of the prefill pair kernels on the default prefill
 # workload (batch 4, 512 tokens onto 3584), from one ncu capture of a sliding and a global
 # layer; used only for that workload and while the kernel sources hash to the recorded value
-NCU_PREFILL_TRAFFIC = {"source_sha1": "7f22685c53dd84dcd5bc968995dcc38f9934436d", "batch": 4, "n_new": 512,
-                       "ctx": 4096, "bytes_per_launch": {"sliding": 73906944 + 2148608,
-                                                         "global": 50576128 + 250112}}
+NCU_PREFILL_TRAFFIC = {"source_sha1": "31b5a94eca65cdc6c26b052c2726d4b1edfad0c9", "batch": 4, "n_new": 512,
+                       "ctx": 4096, "bytes_per_launch": {"sliding": 73969664 + 2414592,
+                                                         "global": 50567936 + 282368}}
 
 
 # ---------------------------------------------------------------------------------------------
