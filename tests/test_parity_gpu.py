@@ -276,6 +276,25 @@ BIG_CLUSTER_SHAPES = [
 ]
 
 
+# latency-bound splits finer than a cluster holds (more than 16 chunks of 32 or 64 keys) whose
+# keys fit 16 chunks of at most 128: coarsened to one 16-chunk cluster, no scratch, no combine
+COARSENED_SHAPES = [
+    (LayerSpec(GLOBAL, 0, 8, 2, 256, False), [2048], 2048),        # E4B's global layers
+    (LayerSpec(GLOBAL, 0, 16, 1, 512, True), [1500, 900], 1536),
+    (LayerSpec(SLIDING, 1500, 8, 4, 128, True), [3000], 3008),
+]
+
+
+@pytest.mark.parametrize("case", range(len(COARSENED_SHAPES)))
+def test_decode_coarsened_to_one_cluster(case):
+    import mixed_sliding_global_gb300 as g
+    spec, lens, cap = COARSENED_SHAPES[case]
+    msl = max(lens)
+    assert g.gemma_attn_workspace_size(len(lens), spec.kind, spec.window, spec.n_q, spec.n_kv,
+                                       spec.head_dim, msl, 1) == 0
+    run_and_compare(one_layer(spec, 1, lens, cap), [0])
+
+
 @pytest.mark.parametrize("case", range(len(BIG_CLUSTER_SHAPES)))
 def test_decode_in_big_clusters(case):
     import mixed_sliding_global_gb300 as g
